@@ -1,0 +1,313 @@
+"""fp64 CPU oracle for exact causal (GQA) self-attention, forward and backward.
+
+TEST INFRASTRUCTURE ONLY. Nothing on the product path imports, calls or links this module:
+only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg use it.
+It shares no code with the CUDA path; both take their inputs from ``workloads``.
+
+What it computes (the plain definition; the head-chunked, trunked method reaches exactly this
+result, only with less memory):
+  * exact attention, every query attending every earlier-or-equal key
+    ["Road to 5 Million Tokens" summary, "The Bottlenecks": quadratic pairwise interactions;
+     "Training Ultra Long Context LM with FPDT", Technical Deep Dive: a query token attends
+     to the keys/values that precede it or are simultaneous];
+  * softmax with the running-maximum statistic the FPDT Technical Deep Dive names; here the
+    maximum is taken over the full row at once (no online merge), which is the definition;
+  * the backward pass is the analytic gradient of that function; P is recomputed from the
+    saved statistic the way FlashAttention-style backward passes recompute it
+    ["Training Ultra Long Context LM with FPDT", Background: the attention backward pass].
+
+Readings where the pages are silent (all from the workload definitions, not the pages):
+  scale = 1/sqrt(D); causal visibility j <= i with S_q = S_k; GQA maps q-head h to kv-head
+  floor(h / (Hq/Hkv)); LSE uses the natural log and is returned as [B, Hq, S].
+
+Layouts: q, dout, o, dq are token-major [B, S, Hq, D]; k, v, dk, dv are [B, S, Hkv, D].
+All arithmetic is numpy float64; inputs of any float dtype are upcast exactly.
+
+Parity status: every public function here is pinned by tests/test_oracle.py (finite
+differences, closed forms, invariants, brute force, a library special case).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+__all__ = [
+    "attn_fwd_ref",
+    "attn_bwd_ref",
+    "attn_rows_ref",
+    "attn_dkdv_window_ref",
+    "attn_fwd_trunked_ref",
+    "attn_bwd_trunked_ref",
+]
+
+
+def _f64(x):
+    """Exact upcast to a float64 numpy array (bf16/fp16 -> fp32 -> fp64 are exact)."""
+    if hasattr(x, "detach"):  # a torch tensor, on any device
+        t = x.detach()
+        if t.is_floating_point() and t.element_size() < 4:
+            t = t.float()
+        return t.cpu().numpy().astype(np.float64, copy=False)
+    return np.asarray(x, dtype=np.float64)
+
+
+def _take(x, b, rows, h):
+    """x[b, rows, h, :] for a numpy array or a torch tensor (rows: int array)."""
+    if hasattr(x, "detach"):
+        import torch
+        return x[b, torch.as_tensor(rows, device=x.device), h, :]
+    return np.asarray(x)[b, rows, h, :]
+
+
+def _shapes(q, k):
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    if Hq % Hkv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    return B, S, Hq, Hkv, D, Hq // Hkv
+
+
+def _scale(D, scale):
+    return 1.0 / math.sqrt(D) if scale is None else float(scale)
+
+
+def _scores(qrows, keys, scale, row_pos, causal):
+    """s_ij = scale * <q_i, k_j>, with keys j > i set to -inf when causal.
+    qrows [n, D] at absolute positions row_pos [n]; keys [m, D] at positions 0..m-1."""
+    s = scale * (qrows @ keys.T)
+    if causal:
+        j = np.arange(keys.shape[0])[None, :]
+        s = np.where(j <= row_pos[:, None], s, -np.inf)
+    return s
+
+
+def _softmax_rows(s):
+    """P = exp(s - max) / sum exp(s - max) over each full row, plus LSE = max + ln(sum)."""
+    mx = s.max(axis=1, keepdims=True)
+    e = np.exp(s - mx)
+    l = e.sum(axis=1, keepdims=True)
+    return e / l, (mx + np.log(l))[:, 0]
+
+
+def attn_fwd_ref(q, k, v, causal=True, scale=None, row_block=512):
+    """O = softmax(scale * Q K^T + causal mask) V per (b, h); LSE per row.
+
+    Returns (o [B,S,Hq,D], lse [B,Hq,S]) in float64."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, S, Hq, Hkv, D, G = _shapes(q, k)
+    sc = _scale(D, scale)
+    o = np.empty((B, S, Hq, D))
+    lse = np.empty((B, Hq, S))
+    for b in range(B):
+        for h in range(Hq):
+            kh = h // G
+            K, V = k[b, :, kh, :], v[b, :, kh, :]
+            for i0 in range(0, S, row_block):
+                i1 = min(S, i0 + row_block)
+                m = i1 if causal else S  # keys beyond the block's last row are all masked
+                s = _scores(q[b, i0:i1, h, :], K[:m], sc, np.arange(i0, i1), causal)
+                P, l = _softmax_rows(s)
+                o[b, i0:i1, h, :] = P @ V[:m]
+                lse[b, h, i0:i1] = l
+    return o, lse
+
+
+def attn_bwd_ref(q, k, v, dout, causal=True, scale=None, row_block=512):
+    """Analytic gradients of O = softmax(scale*QK^T + mask) V, given dO.
+
+    With P recomputed per row block:
+        D_i   = <dO_i, O_i>
+        dP_ij = <dO_i, v_j>
+        dS_ij = P_ij (dP_ij - D_i)
+        dQ_i  = scale * sum_j dS_ij k_j
+        dK_j  = scale * sum_{h in group} sum_i dS_ij q_i
+        dV_j  = sum_{h in group} sum_i P_ij dO_i
+    Returns (o, lse, dq, dk, dv) in float64 (o, lse as in attn_fwd_ref)."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, S, Hq, Hkv, D, G = _shapes(q, k)
+    sc = _scale(D, scale)
+    o = np.empty((B, S, Hq, D))
+    lse = np.empty((B, Hq, S))
+    dq = np.empty((B, S, Hq, D))
+    dk = np.zeros((B, S, Hkv, D))
+    dv = np.zeros((B, S, Hkv, D))
+    for b in range(B):
+        for h in range(Hq):
+            kh = h // G
+            K, V = k[b, :, kh, :], v[b, :, kh, :]
+            for i0 in range(0, S, row_block):
+                i1 = min(S, i0 + row_block)
+                m = i1 if causal else S
+                Qb, dOb = q[b, i0:i1, h, :], do[b, i0:i1, h, :]
+                s = _scores(Qb, K[:m], sc, np.arange(i0, i1), causal)
+                P, l = _softmax_rows(s)
+                Ob = P @ V[:m]
+                o[b, i0:i1, h, :] = Ob
+                lse[b, h, i0:i1] = l
+                Di = np.sum(dOb * Ob, axis=1, keepdims=True)
+                dP = dOb @ V[:m].T
+                dS = P * (dP - Di)
+                dq[b, i0:i1, h, :] = sc * (dS @ K[:m])
+                dk[b, :m, kh, :] += sc * (dS.T @ Qb)
+                dv[b, :m, kh, :] += P.T @ dOb
+    return o, lse, dq, dk, dv
+
+
+def attn_rows_ref(q, k, v, dout, b, h, rows, causal=True, scale=None, row_block=64):
+    """O_i, LSE_i and dQ_i for the query rows ``rows`` of (batch b, q-head h) only.
+
+    Each row is the same definition as attn_bwd_ref restricted to that row (its softmax
+    still runs over the row's full key range); its cost is O(i * D), which makes spot checks
+    at S >= 128K affordable. Rows are processed in sorted blocks so K and V stream through
+    BLAS once per block. Returns (rows_sorted, o [n,D], lse [n], dq [n,D])."""
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    kh = h // (Hq // Hkv)
+    sc = _scale(D, scale)
+    rows = np.asarray(sorted(set(int(r) for r in rows)), dtype=np.int64)
+    m_all = int(rows[-1]) + 1 if causal else S
+    K = _f64(k[b, :m_all, kh, :])
+    V = _f64(v[b, :m_all, kh, :])
+    o = np.empty((len(rows), D))
+    lse = np.empty(len(rows))
+    dq = np.empty((len(rows), D))
+    for n0 in range(0, len(rows), row_block):
+        r = rows[n0:n0 + row_block]
+        m = int(r[-1]) + 1 if causal else S
+        Qb = _f64(_take(q, b, r, h))
+        dOb = _f64(_take(dout, b, r, h))
+        s = _scores(Qb, K[:m], sc, r, causal)
+        P, l = _softmax_rows(s)
+        Ob = P @ V[:m]
+        Di = np.sum(dOb * Ob, axis=1, keepdims=True)
+        dS = P * (dOb @ V[:m].T - Di)
+        o[n0:n0 + len(r)] = Ob
+        lse[n0:n0 + len(r)] = l
+        dq[n0:n0 + len(r)] = sc * (dS @ K[:m])
+    return rows, o, lse, dq
+
+
+def attn_dkdv_window_ref(q, k, v, dout, b, kvh, j0, j1, causal=True, scale=None,
+                         row_block=256):
+    """dK_j and dV_j for key rows j in [j0, j1) of (batch b, kv-head kvh).
+
+    Sums over the G q-heads of the group and over every query row that sees key j
+    (rows i >= j0 when causal); each such row's softmax is taken over its full key range,
+    so the window's result equals the corresponding slice of attn_bwd_ref."""
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    G = Hq // Hkv
+    sc = _scale(D, scale)
+    dk = np.zeros((j1 - j0, D))
+    dv = np.zeros((j1 - j0, D))
+    i_start = j0 if causal else 0
+    K = _f64(k[b, :, kvh, :])
+    V = _f64(v[b, :, kvh, :])
+    for h in range(kvh * G, (kvh + 1) * G):
+        for i0 in range(i_start, S, row_block):
+            i1 = min(S, i0 + row_block)
+            m = max(i1, j1) if causal else S  # window keys past row i are masked to 0
+            Qb = _f64(q[b, i0:i1, h, :])
+            dOb = _f64(dout[b, i0:i1, h, :])
+            s = _scores(Qb, K[:m], sc, np.arange(i0, i1), causal)
+            P, _ = _softmax_rows(s)
+            Ob = P @ V[:m]
+            Di = np.sum(dOb * Ob, axis=1, keepdims=True)
+            Pw = P[:, j0:j1]
+            dSw = Pw * (dOb @ V[j0:j1].T - Di)
+            dk += sc * (dSw.T @ Qb)
+            dv += Pw.T @ dOb
+    return dk, dv
+
+
+# ----------------------------------------------------------------------------------------
+# The head-chunked, trunked formulation. Used only to self-check the merge arithmetic the
+# method relies on: it must reproduce attn_fwd_ref / attn_bwd_ref to fp64 rounding.
+# ----------------------------------------------------------------------------------------
+
+def _trunks(S, T):
+    return [(t0, min(S, t0 + T)) for t0 in range(0, S, T)]
+
+
+def attn_fwd_trunked_ref(q, k, v, head_chunk, seq_trunk, causal=True, scale=None):
+    """UPipe x FPDT forward schedule, written out in fp64.
+
+    For each head group of ``head_chunk`` q-heads ["Road to 5 million sequence length"
+    talk, UPipe passage: compute one set of heads at a time, reusing the buffers], for each
+    query trunk m, fold the key/value trunks n = 0..m (all n when not causal) into running
+    statistics ["Training Ultra Long Context LM with FPDT", Technical Deep Dive: partial
+    output plus maximum-logit statistics updated per trunk]:
+        m_new = max(m_run, rowmax(s));  a = exp(m_run - m_new)
+        l_run = a*l_run + rowsum(exp(s - m_new));  acc = a*acc + exp(s - m_new) V_n
+    and finish with O = acc / l_run, LSE = m_run + ln(l_run)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, S, Hq, Hkv, D, G = _shapes(q, k)
+    if Hq % head_chunk or head_chunk % G:
+        raise ValueError("head_chunk must divide Hq and be a multiple of Hq/Hkv")
+    sc = _scale(D, scale)
+    o = np.empty((B, S, Hq, D))
+    lse = np.empty((B, Hq, S))
+    trunks = _trunks(S, seq_trunk)
+    for g0 in range(0, Hq, head_chunk):
+        for b in range(B):
+            for h in range(g0, g0 + head_chunk):
+                kh = h // G
+                for mi, (q0, q1) in enumerate(trunks):
+                    Qm = q[b, q0:q1, h, :]
+                    acc = np.zeros((q1 - q0, D))
+                    m_run = np.full(q1 - q0, -np.inf)
+                    l_run = np.zeros(q1 - q0)
+                    for ni, (k0, k1) in enumerate(trunks):
+                        if causal and ni > mi:
+                            break
+                        s = sc * (Qm @ k[b, k0:k1, kh, :].T)
+                        if causal and ni == mi:
+                            vis = np.arange(k0, k1)[None, :] <= np.arange(q0, q1)[:, None]
+                            s = np.where(vis, s, -np.inf)
+                        m_new = np.maximum(m_run, s.max(axis=1))
+                        a = np.exp(m_run - m_new)
+                        p = np.exp(s - m_new[:, None])
+                        l_run = a * l_run + p.sum(axis=1)
+                        acc = a[:, None] * acc + p @ v[b, k0:k1, kh, :]
+                        m_run = m_new
+                    o[b, q0:q1, h, :] = acc / l_run[:, None]
+                    lse[b, h, q0:q1] = m_run + np.log(l_run)
+    return o, lse
+
+
+def attn_bwd_trunked_ref(q, k, v, dout, head_chunk, seq_trunk, causal=True, scale=None):
+    """Backward in the same schedule: per head group, per key/value trunk n (outer), per
+    query trunk m >= n (all m when not causal), P recomputed from the forward's LSE:
+        P = exp(s - LSE_i), dS = P (dO V_n^T - D_i), D_i = <dO_i, O_i>,
+        dV_n += P^T dO_m, dK_n += scale dS^T Q_m, dQ_m += scale dS K_n.
+    Returns (o, lse, dq, dk, dv) in float64."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, S, Hq, Hkv, D, G = _shapes(q, k)
+    sc = _scale(D, scale)
+    o, lse = attn_fwd_trunked_ref(q, k, v, head_chunk, seq_trunk, causal, scale)
+    dq = np.zeros((B, S, Hq, D))
+    dk = np.zeros((B, S, Hkv, D))
+    dv = np.zeros((B, S, Hkv, D))
+    trunks = _trunks(S, seq_trunk)
+    for g0 in range(0, Hq, head_chunk):
+        for b in range(B):
+            for h in range(g0, g0 + head_chunk):
+                kh = h // G
+                Dvec = np.sum(do[b, :, h, :] * o[b, :, h, :], axis=1)
+                for ni, (k0, k1) in enumerate(trunks):
+                    Kn, Vn = k[b, k0:k1, kh, :], v[b, k0:k1, kh, :]
+                    for mi, (q0, q1) in enumerate(trunks):
+                        if causal and mi < ni:
+                            continue
+                        Qm, dOm = q[b, q0:q1, h, :], do[b, q0:q1, h, :]
+                        s = sc * (Qm @ Kn.T)
+                        if causal and mi == ni:
+                            vis = np.arange(k0, k1)[None, :] <= np.arange(q0, q1)[:, None]
+                            s = np.where(vis, s, -np.inf)
+                        P = np.exp(s - lse[b, h, q0:q1][:, None])
+                        dS = P * (dOm @ Vn.T - Dvec[q0:q1][:, None])
+                        dv[b, k0:k1, kh, :] += P.T @ dOm
+                        dk[b, k0:k1, kh, :] += sc * (dS.T @ Qm)
+                        dq[b, q0:q1, h, :] += sc * (dS @ Kn)
+    return o, lse, dq, dk, dv
