@@ -1,0 +1,366 @@
+"""Benchmark: causal GQA attention forward + backward on one GB300 (or N independent replicas).
+
+One step = upipe_attn_fwd + upipe_attn_bwd over the whole workload (all head groups, all
+trunks), inputs resident in HBM. Default workload: the Llama3-8B-shaped attention layer at
+S = 131072 (B=1, Hq=32, Hkv=8, D=128, head_chunk=8, seq_trunk=131072, causal), the size the
+throughput target is quoted on. FLOPs follow the FlashAttention benchmark convention:
+fwd = 4*B*Hq*D*S^2/2 (causal), bwd = 2.5 * fwd.
+
+Prints ONE JSON line (rank 0). Under torchrun every rank runs an independent replica on its own
+GPU (the path does not shard on one box); value = total FLOPs of all ranks / max rank time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--head-chunk H] [--seq-trunk T] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("causal attn fwd+bwd TFLOP/s & % BF16 tensor peak on 1 GB300; peak workspace GB")
+UNIT = "TFLOP/s"
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="llama8b_s128k")
+    ap.add_argument("--head-chunk", type=int, default=None)
+    ap.add_argument("--seq-trunk", type=int, default=None)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, \
+            "fallback"
+
+
+# ---- clocks sampled during the timed region ------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "200"], stdout=open(self.path, "w"),
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[4:]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for _, _, _, f in rows for n, v in zip(names, f[1:]) if v == "Active"})
+        load = [r for r in rows if r[2] > 200.0] or rows
+        return {"sm_mhz": statistics.median(r[0] for r in load),
+                "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows),
+                "samples": len(rows), "reasons": reasons}
+
+
+# ---- the CPU oracle on a bounded sample ----------------------------------------------------
+def oracle_sample(w, S_sample, inputs=None):
+    """Times the fp64 oracle's forward + backward on the first S_sample tokens of the workload
+    (an exact causal sub-problem). Returns (tflops, seconds, flops, description, cores)."""
+    import numpy as np
+    import oracle
+    from workloads import make_inputs
+    if inputs is not None:
+        q, k, v, do = (t[:, :S_sample].float().cpu().numpy().astype(np.float64) for t in inputs)
+        src = "prefix of the seeded workload tensors"
+    else:
+        ws = w.with_(S=S_sample)
+        q, k, v, do = (t.float().numpy().astype(np.float64) for t in make_inputs(ws, "cpu"))
+        src = "same recipe regenerated on the CPU at the sample length"
+    flops = 3.5 * w.with_(S=S_sample).flops_fwd()
+    t0 = time.perf_counter()
+    oracle.attn_bwd_ref(q, k, v, do, causal=w.causal)
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    desc = (f"fp64 numpy oracle fwd+bwd on the first {S_sample} of {w.S} tokens, all {w.Hq} "
+            f"q-heads ({src}); FLOPs by the same causal convention")
+    return flops / dt / 1e12, dt, flops, desc, cores
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def run_reference(a):
+    """The reference arm: the fp64 oracle on the host cores, rank 0 only."""
+    rank, world, _ = _dist()
+    if rank != 0:
+        return
+    from workloads import WORKLOADS
+    w = WORKLOADS[a.workload]
+    S_sample = min(w.S, 1024)
+    vals = []
+    for i in range(a.warmup + a.steps):
+        tf, dt, flops, desc, cores = oracle_sample(w, S_sample)
+        if i >= a.warmup:
+            vals.append((tf, dt))
+    value = sum(flops for _ in vals) / sum(dt for _, dt in vals) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": 1000.0 * statistics.mean(dt for _, dt in vals),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+                   "head_chunk": a.head_chunk or w.head_chunk,
+                   "seq_trunk": a.seq_trunk or w.seq_trunk, "causal": w.causal,
+                   "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(a):
+    import torch
+    import torch.distributed as dist
+
+    import context_parallelism_gb300 as up
+    from workloads import WORKLOADS, make_inputs
+
+    rank, world, local = _dist()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = WORKLOADS[a.workload]
+    hc = a.head_chunk or w.head_chunk
+    T = a.seq_trunk or w.seq_trunk
+    kv_host = w.kv_on_host
+    B, S, Hq, Hkv, D = w.B, w.S, w.Hq, w.Hkv, w.D
+
+    q, k, v, do = make_inputs(w, str(dev) if w.gen_device == "cuda" else "cpu")
+    q, do = q.to(dev), do.to(dev)
+    if kv_host:
+        kh = torch.empty(k.shape, dtype=k.dtype, pin_memory=True); kh.copy_(k)
+        vh = torch.empty(v.shape, dtype=v.dtype, pin_memory=True); vh.copy_(v)
+        k_in, v_in = kh, vh
+    else:
+        k_in, v_in = k.to(dev), v.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device=dev)
+    dq = torch.empty_like(q)
+    dk = torch.empty((B, S, Hkv, D), dtype=q.dtype, device=dev)
+    dv = torch.empty_like(dk)
+    ws_bytes = up.upipe_workspace_bytes(B, S, Hq, Hkv, D, 1, hc, T, up.UPIPE_PASS_BOTH, kv_host)
+    ws_full = up.upipe_workspace_bytes(B, S, Hq, Hkv, D, 1, Hq, T, up.UPIPE_PASS_BOTH, kv_host)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        up.upipe_attn_fwd(q, k_in, v_in, o, lse, B, S, Hq, Hkv, D, 1, hc, T, ws, ws_bytes, stream)
+        up.upipe_attn_bwd(q, k_in, v_in, o, lse, do, dq, dk, dv, B, S, Hq, Hkv, D, 1, hc, T, ws,
+                          ws_bytes, stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(a.warmup):
+        step()
+    up.upipe_sync_status(stream)
+
+    # ---- timed region: K steps, device events on the launching stream ----
+    fwd_ms = bwd_ms = 0.0
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
+    up.upipe_profile_read()  # drop anything recorded before
+    up.upipe_profile_enable(True)
+    clocks = ClockSampler(local)
+    barrier()
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = up.upipe_launch_count()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(a.steps):
+        ev[i][0].record(stream)
+        up.upipe_attn_fwd(q, k_in, v_in, o, lse, B, S, Hq, Hkv, D, 1, hc, T, ws, ws_bytes, stream)
+        ev[i][1].record(stream)
+        up.upipe_attn_bwd(q, k_in, v_in, o, lse, do, dq, dk, dv, B, S, Hq, Hkv, D, 1, hc, T, ws,
+                          ws_bytes, stream)
+        ev[i][2].record(stream)
+    t_end.record(stream)
+    barrier()
+    launches = up.upipe_launch_count() - launches0
+    clk = clocks.stop()
+    up.upipe_profile_enable(False)
+    prof = up.upipe_profile_read()
+    up.upipe_sync_status(stream)
+    elapsed = t_start.elapsed_time(t_end)
+    for e0, e1, e2 in ev:
+        fwd_ms += e0.elapsed_time(e1)
+        bwd_ms += e1.elapsed_time(e2)
+    t_max = elapsed
+    if world > 1:
+        tt = torch.tensor([elapsed], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_max = float(tt.item())
+    ms_per_step = t_max / a.steps
+    f_fwd, f_bwd = w.flops_fwd(), w.flops_bwd()
+    value = world * (f_fwd + f_bwd) * a.steps / (t_max / 1e3) / 1e12
+    peaks, peak_src = _peaks()
+    peak = float(peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"])
+
+    # dominant kernel: the class with the most device time; its algorithmic FLOPs are the
+    # causal FLOPs of the pass it belongs to (all of them run inside that kernel class)
+    algo = {"attn_fwd": f_fwd * a.steps, "attn_bwd": f_bwd * a.steps}
+    top = max(prof, key=lambda kname: prof[kname][0])
+    tot_ms, n_launch = prof[top]
+    if top in algo and tot_ms > 0:
+        achieved = algo[top] / (tot_ms / 1e3) / 1e12
+        roofline = {"kernel": top, "bound": "tensor", "achieved": achieved, "peak": peak,
+                    "unit": "TFLOP/s", "frac": achieved / peak,
+                    "peak_source": f"{peak_src} bf16_tflops_sustained",
+                    "launches": n_launch, "avg_launch_ms": tot_ms / max(n_launch, 1),
+                    "traffic": None}
+    else:
+        roofline = {"kernel": top, "bound": "hbm", "achieved": None, "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": None, "traffic": None}
+    kernels = {kname: {"ms_per_step": t / a.steps, "launches_per_step": n / a.steps}
+               for kname, (t, n) in prof.items() if n}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,%g) bf16, no weights)" % w.std,
+        "config": {"workload": w.name, "B": B, "S": S, "Hq": Hq, "Hkv": Hkv, "D": D,
+                   "head_chunk": hc, "seq_trunk": T, "causal": True, "kv_on_host": kv_host,
+                   "l2": "inputs larger than L2 (q is %.2f GiB)" % (q.nbytes / 2**30),
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "fwd_tflops": world * f_fwd * a.steps / (fwd_ms / 1e3) / 1e12,
+        "bwd_tflops": world * f_bwd * a.steps / (bwd_ms / 1e3) / 1e12,
+        "frac_of_bf16_peak": value / world / peak,
+        "peak_tflops": peak, "peak_source": peak_src,
+        "workspace_gb": ws_bytes / 1e9, "workspace_unchunked_gb": ws_full / 1e9,
+        "workspace_ratio": ws_bytes / ws_full,
+        "roofline": roofline, "kernels": kernels,
+        "gpu_launches": int(launches), "clocks": clk,
+    }
+
+    # ---- end to end: host buffers in, results out, copies inside the timed region ----
+    if not a.no_e2e:
+        hq = torch.empty(q.shape, dtype=q.dtype, pin_memory=True); hq.copy_(q)
+        hdo = torch.empty(do.shape, dtype=do.dtype, pin_memory=True); hdo.copy_(do)
+        if kv_host:
+            hk, hv = k_in, v_in
+        else:
+            hk = torch.empty(k.shape, dtype=k.dtype, pin_memory=True); hk.copy_(k_in)
+            hv = torch.empty(v.shape, dtype=v.dtype, pin_memory=True); hv.copy_(v_in)
+        outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse, dq, dk, dv)]
+        h2d = hq.nbytes + hdo.nbytes + (0 if kv_host else hk.nbytes + hv.nbytes)
+        d2h = sum(t.nbytes for t in outs_h)
+
+        def e2e_step():
+            q.copy_(hq, non_blocking=True)
+            do.copy_(hdo, non_blocking=True)
+            if not kv_host:
+                k_in.copy_(hk, non_blocking=True)
+                v_in.copy_(hv, non_blocking=True)
+            up.upipe_attn_fwd(q, k_in, v_in, o, lse, B, S, Hq, Hkv, D, 1, hc, T, ws, ws_bytes, stream)
+            up.upipe_attn_bwd(q, k_in, v_in, o, lse, do, dq, dk, dv, B, S, Hq, Hkv, D, 1, hc, T,
+                              ws, ws_bytes, stream)
+            for hdst, dsrc in zip(outs_h, (o, lse, dq, dk, dv)):
+                hdst.copy_(dsrc, non_blocking=True)
+
+        e2e_step()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(a.steps):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        te = e0.elapsed_time(e1)
+        if world > 1:
+            tt = torch.tensor([te], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            te = float(tt.item())
+        line["e2e"] = {"value": world * (f_fwd + f_bwd) * a.steps / (te / 1e3) / 1e12,
+                       "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                       "d2h_bytes_per_step": int(d2h)}
+        up.upipe_sync_status(stream)
+
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        tf, dt, flops, desc, cores = oracle_sample(w, min(S, 2048), (q, k, v, do))
+        line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": desc, "seconds": dt}
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    a = _args()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_ours(a)
+
+
+if __name__ == "__main__":
+    main()

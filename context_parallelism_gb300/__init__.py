@@ -1,0 +1,239 @@
+"""Python binding of libupipe: head-chunked, trunked causal (GQA) attention for one GB300.
+
+Argument marshalling only: every step of the attention path runs in the library's CUDA
+kernels, reached through the C ABI declared in ``include/upipe.h``. The functions named
+``upipe_*`` mirror that ABI one to one (tensors may be passed where the ABI takes pointers);
+``attention_forward`` / ``attention_backward`` allocate outputs and the workspace with torch
+and call them. There is no fallback: if ``libupipe.so`` is missing, importing the binding
+fails with an error that says how to build it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as _np  # noqa: F401  (kept for users that pass numpy-backed pinned buffers)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libupipe.so")
+
+UPIPE_OK = 0
+UPIPE_ERR_INVALID_ARG = 1
+UPIPE_ERR_UNSUPPORTED = 2
+UPIPE_ERR_WORKSPACE_TOO_SMALL = 3
+UPIPE_ERR_CUDA = 4
+UPIPE_ERR_TIMEOUT = 5
+
+UPIPE_PASS_FWD, UPIPE_PASS_BWD, UPIPE_PASS_BOTH = 0, 1, 2
+
+KERNEL_CLASSES = ["layout", "attn_fwd", "bwd_pre", "attn_bwd", "dq_convert", "other"]
+
+# Every symbol include/upipe.h declares, with (restype, argtypes).
+_vp, _i, _i64, _sz, _u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_uint64
+
+
+class KernelStat(ctypes.Structure):
+    _fields_ = [("total_ms", ctypes.c_double), ("launches", ctypes.c_uint64)]
+
+
+SIGNATURES = {
+    "upipe_workspace_bytes": (_sz, [_i, _i64, _i, _i, _i, _i, _i, _i64, _i, _i]),
+    "upipe_attn_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i64, _i, _i, _i, _i, _i, _i64, _vp,
+                            _sz, _vp]),
+    "upipe_attn_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i64, _i, _i, _i,
+                            _i, _i, _i64, _vp, _sz, _vp]),
+    "upipe_seq_to_head_major": (_i, [_vp, _vp, _i, _i64, _i, _i, _i, _i, _vp]),
+    "upipe_head_to_seq_major": (_i, [_vp, _vp, _i, _i64, _i, _i, _i, _i, _vp]),
+    "upipe_sync_status": (_i, [_vp]),
+    "upipe_status_string": (ctypes.c_char_p, [_i]),
+    "upipe_last_error_message": (ctypes.c_char_p, []),
+    "upipe_shutdown": (None, []),
+    "upipe_launch_count": (_u64, []),
+    "upipe_profile_enable": (_i, [_i]),
+    "upipe_profile_read": (_i, [ctypes.POINTER(KernelStat), _i]),
+    "upipe_selftest_umma": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp]),
+    "upipe_selftest_wait_timeout": (_i, [_i, _vp]),
+}
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with `python -c \"import __graft_entry__ as g; "
+            f"g.build()\"` (or `python context_parallelism_gb300/build.py`)")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+class UpipeError(RuntimeError):
+    def __init__(self, status, where):
+        msg = _lib.upipe_last_error_message().decode()
+        name = _lib.upipe_status_string(status).decode()
+        super().__init__(f"{where}: {name}: {msg}")
+        self.status = status
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    raise TypeError(f"cannot pass {type(x)} as a pointer")
+
+
+def _stream(stream, *tensors):
+    if stream is not None:
+        return stream if isinstance(stream, int) else stream.cuda_stream
+    import torch
+    for t in tensors:
+        if hasattr(t, "is_cuda") and t.is_cuda:
+            return torch.cuda.current_stream(t.device).cuda_stream
+    return None
+
+
+def _check(status, where):
+    if status != UPIPE_OK:
+        raise UpipeError(status, where)
+
+
+# ---- one-to-one ABI wrappers ------------------------------------------------------------
+
+def upipe_workspace_bytes(B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk, pass_=UPIPE_PASS_BOTH,
+                          kv_on_host=0):
+    return int(_lib.upipe_workspace_bytes(B, S, Hq, Hkv, D, int(causal), head_chunk, seq_trunk,
+                                          pass_, int(kv_on_host)))
+
+
+def upipe_attn_fwd(q, k, v, o, lse, B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk, workspace,
+                   workspace_bytes=None, stream=None):
+    wb = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    st = _lib.upipe_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, S, Hq, Hkv, D,
+                             int(causal), head_chunk, seq_trunk, _ptr(workspace), wb,
+                             _stream(stream, q, o))
+    _check(st, "upipe_attn_fwd")
+
+
+def upipe_attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, S, Hq, Hkv, D, causal, head_chunk,
+                   seq_trunk, workspace, workspace_bytes=None, stream=None):
+    wb = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    st = _lib.upipe_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                             _ptr(dk), _ptr(dv), B, S, Hq, Hkv, D, int(causal), head_chunk,
+                             seq_trunk, _ptr(workspace), wb, _stream(stream, q, dq))
+    _check(st, "upipe_attn_bwd")
+
+
+def upipe_seq_to_head_major(src, dst, B, S, H, D, h_begin, h_count, stream=None):
+    _check(_lib.upipe_seq_to_head_major(_ptr(src), _ptr(dst), B, S, H, D, h_begin, h_count,
+                                        _stream(stream, src)), "upipe_seq_to_head_major")
+
+
+def upipe_head_to_seq_major(src, dst, B, S, H, D, h_begin, h_count, stream=None):
+    _check(_lib.upipe_head_to_seq_major(_ptr(src), _ptr(dst), B, S, H, D, h_begin, h_count,
+                                        _stream(stream, src)), "upipe_head_to_seq_major")
+
+
+def upipe_sync_status(stream=None):
+    """Synchronise the stream and raise UpipeError if a kernel's bounded wait expired."""
+    import torch
+    s = stream if stream is not None else (torch.cuda.current_stream().cuda_stream
+                                           if torch.cuda.is_available() else None)
+    if s is not None and not isinstance(s, int):
+        s = s.cuda_stream
+    _check(_lib.upipe_sync_status(s), "upipe_sync_status")
+
+
+def upipe_status_string(status):
+    return _lib.upipe_status_string(status).decode()
+
+
+def upipe_last_error_message():
+    return _lib.upipe_last_error_message().decode()
+
+
+def upipe_shutdown():
+    _lib.upipe_shutdown()
+
+
+def upipe_launch_count():
+    return int(_lib.upipe_launch_count())
+
+
+def upipe_profile_enable(on=True):
+    _check(_lib.upipe_profile_enable(int(on)), "upipe_profile_enable")
+
+
+def upipe_profile_read():
+    """Returns {class name: (total_ms, launches)} for the launches recorded since last read."""
+    arr = (KernelStat * len(KERNEL_CLASSES))()
+    _check(_lib.upipe_profile_read(arr, len(KERNEL_CLASSES)), "upipe_profile_read")
+    return {n: (arr[i].total_ms, int(arr[i].launches)) for i, n in enumerate(KERNEL_CLASSES)}
+
+
+def upipe_selftest_umma(a, b, c, N, K, a_mn_major, b_mn_major, a_manual=0, lbo=16384, sbo=1024,
+                        stream=None):
+    _check(_lib.upipe_selftest_umma(_ptr(a), _ptr(b), _ptr(c), N, K, int(a_mn_major),
+                                    int(b_mn_major), int(a_manual), lbo, sbo,
+                                    _stream(stream, a)), "upipe_selftest_umma")
+
+
+def upipe_selftest_wait_timeout(limit_us, stream=None):
+    _check(_lib.upipe_selftest_wait_timeout(limit_us, _stream(stream)),
+           "upipe_selftest_wait_timeout")
+
+
+# ---- convenience: allocate outputs / workspace with torch, then call the ABI -------------
+
+def _dims(q, k):
+    B, S, Hq, D = q.shape
+    return B, S, Hq, k.shape[2], D
+
+
+def attention_forward(q, k, v, causal=True, head_chunk=None, seq_trunk=None, workspace=None,
+                      stream=None):
+    """o, lse = attention over token-major bf16 q [B,S,Hq,D], k/v [B,S,Hkv,D].
+    k/v may be pinned host tensors (staged trunk by trunk)."""
+    import torch
+    B, S, Hq, Hkv, D = _dims(q, k)
+    hc = head_chunk or Hq
+    T = seq_trunk or S
+    kv_host = not k.is_cuda
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    need = upipe_workspace_bytes(B, S, Hq, Hkv, D, causal, hc, T, UPIPE_PASS_FWD, kv_host)
+    if need == 0:
+        upipe_attn_fwd(q, k, v, o, lse, B, S, Hq, Hkv, D, causal, hc, T, 0, 0, stream)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    upipe_attn_fwd(q, k, v, o, lse, B, S, Hq, Hkv, D, causal, hc, T, workspace, None, stream)
+    return o, lse
+
+
+def attention_backward(q, k, v, o, lse, dout, causal=True, head_chunk=None, seq_trunk=None,
+                       workspace=None, stream=None):
+    """dq, dk, dv for the forward above (dk/dv are device tensors even for host k/v)."""
+    import torch
+    B, S, Hq, Hkv, D = _dims(q, k)
+    hc = head_chunk or Hq
+    T = seq_trunk or S
+    kv_host = not k.is_cuda
+    dq = torch.empty_like(q)
+    dk = torch.empty((B, S, Hkv, D), dtype=q.dtype, device=q.device)
+    dv = torch.empty((B, S, Hkv, D), dtype=q.dtype, device=q.device)
+    need = upipe_workspace_bytes(B, S, Hq, Hkv, D, causal, hc, T, UPIPE_PASS_BWD, kv_host)
+    if need == 0:
+        upipe_attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, S, Hq, Hkv, D, causal, hc, T, 0, 0,
+                       stream)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    upipe_attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, S, Hq, Hkv, D, causal, hc, T, workspace,
+                   None, stream)
+    return dq, dk, dv

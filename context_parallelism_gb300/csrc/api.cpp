@@ -1,0 +1,713 @@
+// C ABI, argument validation, workspace plan and the head-group x sequence-trunk scheduler.
+//
+// Schedule (per call):
+//   for each head group g of head_chunk q-heads (UPipe: one set of heads at a time, all groups
+//   reusing one workspace - "Road to 5 million sequence length" talk, UPipe passage;
+//   "Road to 5 Million Tokens" summary, section 2 item 6):
+//     gather the group's Q (and K/V when they are on the device) into head-major workspace
+//     (the single-GPU stand-in for the Ulysses all-to-all);
+//     forward: for each query trunk m, fold key/value trunks n = 0..m (all n if not causal)
+//       into running softmax state, finalising O and LSE on the last one (FPDT Technical Deep
+//       Dive: Q_m attends K_1..K_m, statistics updated per trunk);
+//     backward: pre-pass (dO gather, D = rowsum(dO*O), LSE prescale, zero dQ accumulator),
+//       then one launch per key/value trunk n over all query rows that see it, then the dQ
+//       conversion.
+//   When K/V are pinned host memory every trunk is copied into one of two device slots on an
+//   internal copy stream, one trunk ahead of the compute stream, with events ordering slot
+//   reuse (FPDT Key Findings items 2-3 and Technical Deep Dive: host offload + double buffer,
+//   separate streams for compute and host<->device copies).
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/upipe.h"
+#include "internal.h"
+
+namespace upipe {
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int status, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return status;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(UPIPE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define UPIPE_CUDA(call)                                  \
+  do {                                                    \
+    cudaError_t e_ = (call);                              \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #call);   \
+  } while (0)
+
+// ---- per-device state -----------------------------------------------------------------------
+struct DevState {
+  bool ready = false;
+  cudaStream_t copy = nullptr;
+  cudaEvent_t slot_ready[2] = {nullptr, nullptr};
+  cudaEvent_t slot_free[2] = {nullptr, nullptr};
+  cudaEvent_t entry = nullptr;
+  uint32_t* err = nullptr;  // 256-byte status word allocation
+};
+constexpr int kMaxDev = 64;
+std::mutex g_mu;
+DevState g_dev[kMaxDev];
+
+int dev_state(int dev, DevState** out) {
+  if (dev < 0 || dev >= kMaxDev) return fail(UPIPE_ERR_UNSUPPORTED, "device %d", dev);
+  DevState& d = g_dev[dev];
+  if (!d.ready) {
+    UPIPE_CUDA(cudaStreamCreateWithFlags(&d.copy, cudaStreamNonBlocking));
+    for (int i = 0; i < 2; ++i) {
+      UPIPE_CUDA(cudaEventCreateWithFlags(&d.slot_ready[i], cudaEventDisableTiming));
+      UPIPE_CUDA(cudaEventCreateWithFlags(&d.slot_free[i], cudaEventDisableTiming));
+    }
+    UPIPE_CUDA(cudaEventCreateWithFlags(&d.entry, cudaEventDisableTiming));
+    UPIPE_CUDA(cudaMalloc(&d.err, 256));
+    UPIPE_CUDA(cudaMemset(d.err, 0, 256));
+    UPIPE_CUDA(cudaDeviceSynchronize());
+    d.ready = true;
+  }
+  *out = &d;
+  return UPIPE_OK;
+}
+
+// ---- launch accounting / profiling ----------------------------------------------------------
+std::atomic<uint64_t> g_launches{0};
+std::atomic<bool> g_profile{false};
+struct ProfRec {
+  int kclass;
+  cudaEvent_t e0, e1;
+};
+std::mutex g_prof_mu;
+std::vector<ProfRec> g_prof;
+std::vector<cudaEvent_t> g_event_pool;
+thread_local cudaEvent_t g_pending_e0 = nullptr;
+
+cudaEvent_t pool_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+}  // namespace
+
+void launch_begin(int kclass, cudaStream_t stream) {
+  (void)kclass;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (!g_profile.load(std::memory_order_relaxed)) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_pending_e0 = pool_event();
+  if (g_pending_e0) cudaEventRecord(g_pending_e0, stream);
+}
+
+void launch_end(int kclass, cudaStream_t stream) {
+  if (!g_profile.load(std::memory_order_relaxed) || !g_pending_e0) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  cudaEvent_t e1 = pool_event();
+  if (!e1) return;
+  cudaEventRecord(e1, stream);
+  g_prof.push_back({kclass, g_pending_e0, e1});
+  g_pending_e0 = nullptr;
+}
+
+// ---- tensor maps ----------------------------------------------------------------------------
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+}  // namespace
+
+cudaError_t make_tmap_bf16(CUtensorMap* map, const void* base, int64_t cols, int64_t rows,
+                           int64_t depth) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(depth)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols * 2),
+                                 static_cast<cuuint64_t>(cols * rows * 2)};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+namespace {
+
+// ---- workspace plan ---------------------------------------------------------------------------
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct Plan {
+  int B = 0, Hq = 0, Hkv = 0, D = 0, G = 0, hc = 0, kc = 0, causal = 1;
+  int64_t S = 0, T = 0, S_pad = 0, T_pad = 0;
+  int n_trunks = 0;
+  bool kv_host = false;
+  // forward segments
+  size_t f_qw = 0, f_kw = 0, f_vw = 0, f_slot_k[2] = {0, 0}, f_slot_v[2] = {0, 0};
+  size_t f_state_o = 0, f_state_ml = 0, f_total = 0;
+  // backward segments
+  size_t b_qw = 0, b_dow = 0, b_kw = 0, b_vw = 0, b_slot_k[2] = {0, 0}, b_slot_v[2] = {0, 0};
+  size_t b_dqacc = 0, b_lse2 = 0, b_dvec = 0, b_total = 0;
+};
+
+// Validates shapes (no device access). Returns UPIPE_OK and fills the plan.
+int make_plan(int B, int64_t S, int Hq, int Hkv, int D, int causal, int head_chunk,
+              int64_t seq_trunk, int kv_on_host, Plan* p) {
+  if (B < 1 || S < 1 || Hq < 1 || Hkv < 1 || D < 1)
+    return fail(UPIPE_ERR_INVALID_ARG, "sizes must be positive (B=%d S=%lld Hq=%d Hkv=%d D=%d)",
+                B, static_cast<long long>(S), Hq, Hkv, D);
+  if (Hq % Hkv) return fail(UPIPE_ERR_INVALID_ARG, "Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
+  const int G = Hq / Hkv;
+  if (head_chunk < 1 || Hq % head_chunk)
+    return fail(UPIPE_ERR_INVALID_ARG, "head_chunk=%d must divide Hq=%d", head_chunk, Hq);
+  if (head_chunk % G)
+    return fail(UPIPE_ERR_INVALID_ARG,
+                "head_chunk=%d must be a multiple of Hq/Hkv=%d (a group owns whole kv-heads)",
+                head_chunk, G);
+  if (causal != 0 && causal != 1) return fail(UPIPE_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (seq_trunk < 1) return fail(UPIPE_ERR_INVALID_ARG, "seq_trunk must be >= 1");
+  if (D != 64 && D != 128) return fail(UPIPE_ERR_UNSUPPORTED, "D=%d (supported: 64, 128)", D);
+  if (S > (int64_t(1) << 30)) return fail(UPIPE_ERR_UNSUPPORTED, "S=%lld > 2^30", (long long)S);
+  const int64_t T = seq_trunk >= S ? S : seq_trunk;
+  if (T < S && T % 128)
+    return fail(UPIPE_ERR_INVALID_ARG, "seq_trunk=%lld must be a multiple of 128 when < S",
+                static_cast<long long>(seq_trunk));
+  p->B = B; p->Hq = Hq; p->Hkv = Hkv; p->D = D; p->G = G; p->hc = head_chunk;
+  p->kc = head_chunk / G; p->causal = causal; p->S = S; p->T = T;
+  p->S_pad = (S + 127) / 128 * 128;
+  p->T_pad = (T + 127) / 128 * 128;
+  p->n_trunks = static_cast<int>((S + T - 1) / T);
+  p->kv_host = kv_on_host != 0;
+
+  const size_t hcB = static_cast<size_t>(B) * p->hc, kcB = static_cast<size_t>(B) * p->kc;
+  const size_t qw = hcB * S * D * 2, kvw = kcB * S * D * 2, slot = kcB * T * D * 2;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes);
+    return at;
+  };
+  // forward
+  p->f_qw = take(qw);
+  if (p->kv_host) {
+    for (int i = 0; i < 2; ++i) { p->f_slot_k[i] = take(slot); p->f_slot_v[i] = take(slot); }
+  } else {
+    p->f_kw = take(kvw);
+    p->f_vw = take(kvw);
+  }
+  if (p->n_trunks > 1) {
+    p->f_state_o = take(hcB * p->T_pad * D * 4);
+    p->f_state_ml = take(hcB * p->T_pad * 2 * 4);
+  }
+  p->f_total = off;
+  // backward
+  off = 0;
+  p->b_qw = take(qw);
+  p->b_dow = take(qw);
+  if (p->kv_host) {
+    for (int i = 0; i < 2; ++i) { p->b_slot_k[i] = take(slot); p->b_slot_v[i] = take(slot); }
+  } else {
+    p->b_kw = take(kvw);
+    p->b_vw = take(kvw);
+  }
+  p->b_dqacc = take(hcB * p->S_pad * D * 4);
+  p->b_lse2 = take(hcB * p->S_pad * 4);
+  p->b_dvec = take(hcB * p->S_pad * 4);
+  p->b_total = off;
+  return UPIPE_OK;
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+// Where a pointer lives. kind: 0 device (of *dev), 1 pinned host, -1 pageable/unknown.
+int pointer_kind(const void* ptr, int* dev) {
+  cudaPointerAttributes at;
+  cudaError_t e = cudaPointerGetAttributes(&at, ptr);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  if (at.type == cudaMemoryTypeDevice) {
+    *dev = at.device;
+    return 0;
+  }
+  if (at.type == cudaMemoryTypeHost) return 1;
+  return -1;
+}
+
+// Checks placement of the token-major tensors; selects the device. kv_host out.
+int check_placement(const void* const* dev_ptrs, int n_dev, const char* const* names,
+                    const void* k, const void* v, bool* kv_host, int* device) {
+  int dev0 = -1;
+  for (int i = 0; i < n_dev; ++i) {
+    int d = -1;
+    if (pointer_kind(dev_ptrs[i], &d) != 0)
+      return fail(UPIPE_ERR_INVALID_ARG, "%s must be device memory", names[i]);
+    if (dev0 < 0) dev0 = d;
+    if (d != dev0) return fail(UPIPE_ERR_INVALID_ARG, "%s is on device %d, not %d", names[i], d, dev0);
+  }
+  int dk = -1, dv = -1;
+  const int kk = pointer_kind(k, &dk), kv = pointer_kind(v, &dv);
+  if (kk < 0 || kv < 0)
+    return fail(UPIPE_ERR_INVALID_ARG, "k and v must be device memory or pinned host memory");
+  if (kk != kv) return fail(UPIPE_ERR_INVALID_ARG, "k and v must both be on the device or both pinned on the host");
+  if (kk == 0 && (dk != dev0 || dv != dev0))
+    return fail(UPIPE_ERR_INVALID_ARG, "k/v are on another device");
+  *kv_host = (kk == 1);
+  *device = dev0;
+  return UPIPE_OK;
+}
+
+// Host -> device copy of one key/value trunk [n*T, n*T+Tn) of kv-heads kvh0..kvh0+kc into a
+// slot laid out [B*kc][Tn][D]. The 2-D copy does the head gather.
+int stage_trunk(const Plan& p, const void* src, uint8_t* slot, int kvh0, int64_t t0, int64_t Tn,
+                cudaStream_t copy) {
+  const size_t row = static_cast<size_t>(p.D) * 2;
+  for (int b = 0; b < p.B; ++b)
+    for (int c = 0; c < p.kc; ++c) {
+      const uint8_t* s = static_cast<const uint8_t*>(src) +
+                         ((static_cast<size_t>(b) * p.S + t0) * p.Hkv + kvh0 + c) * row;
+      uint8_t* d = slot + (static_cast<size_t>(b) * p.kc + c) * Tn * row;
+      UPIPE_CUDA(cudaMemcpy2DAsync(d, row, s, static_cast<size_t>(p.Hkv) * row, row,
+                                   static_cast<size_t>(Tn), cudaMemcpyHostToDevice, copy));
+    }
+  return UPIPE_OK;
+}
+
+// Double-buffered trunk stager shared by forward and backward.
+struct Stager {
+  const Plan& p;
+  DevState* ds;
+  cudaStream_t compute;
+  const void* k;
+  const void* v;
+  uint8_t* slot_k[2];
+  uint8_t* slot_v[2];
+  struct Job { int kvh0; int n; };
+  std::vector<Job> jobs;
+  int staged = 0;  // jobs whose copies are enqueued
+
+  int enqueue_copy(int i) {
+    const Job& j = jobs[i];
+    const int s = i & 1;
+    const int64_t t0 = static_cast<int64_t>(j.n) * p.T;
+    const int64_t Tn = std::min<int64_t>(p.T, p.S - t0);
+    UPIPE_CUDA(cudaStreamWaitEvent(ds->copy, ds->slot_free[s], 0));
+    int st = stage_trunk(p, k, slot_k[s], j.kvh0, t0, Tn, ds->copy);
+    if (st != UPIPE_OK) return st;
+    st = stage_trunk(p, v, slot_v[s], j.kvh0, t0, Tn, ds->copy);
+    if (st != UPIPE_OK) return st;
+    UPIPE_CUDA(cudaEventRecord(ds->slot_ready[s], ds->copy));
+    return UPIPE_OK;
+  }
+  // Before the kernel of job i: its copy (and the next one, as prefetch) are enqueued and the
+  // compute stream waits for slot i%2.
+  int before(int i) {
+    while (staged <= i + 1 && staged < static_cast<int>(jobs.size())) {
+      const int st = enqueue_copy(staged);
+      if (st != UPIPE_OK) return st;
+      ++staged;
+    }
+    UPIPE_CUDA(cudaStreamWaitEvent(compute, ds->slot_ready[i & 1], 0));
+    return UPIPE_OK;
+  }
+  int after(int i) {
+    UPIPE_CUDA(cudaEventRecord(ds->slot_free[i & 1], compute));
+    return UPIPE_OK;
+  }
+};
+
+}  // namespace
+}  // namespace upipe
+
+using namespace upipe;
+
+extern "C" {
+
+size_t upipe_workspace_bytes(int B, int64_t S, int Hq, int Hkv, int D, int causal,
+                             int head_chunk, int64_t seq_trunk, int pass, int kv_on_host) {
+  Plan p;
+  if (make_plan(B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk, kv_on_host, &p) != UPIPE_OK)
+    return 0;
+  if (pass == UPIPE_PASS_FWD) return p.f_total;
+  if (pass == UPIPE_PASS_BWD) return p.b_total;
+  if (pass == UPIPE_PASS_BOTH) return std::max(p.f_total, p.b_total);
+  return 0;
+}
+
+int upipe_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                   int64_t S, int Hq, int Hkv, int D, int causal, int head_chunk,
+                   int64_t seq_trunk, void* workspace, size_t workspace_bytes, void* stream_) {
+  g_last_error.clear();
+  if (!q || !k || !v || !o || !lse || !workspace)
+    return fail(UPIPE_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return fail(UPIPE_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(workspace) % kAlign)
+    return fail(UPIPE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  Plan p0;
+  int st = make_plan(B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk, 0, &p0);
+  if (st != UPIPE_OK) return st;
+  const void* dptrs[4] = {q, o, lse, workspace};
+  const char* names[4] = {"q", "o", "lse", "workspace"};
+  bool kv_host = false;
+  int dev = 0;
+  st = check_placement(dptrs, 4, names, k, v, &kv_host, &dev);
+  if (st != UPIPE_OK) return st;
+  Plan p;
+  make_plan(B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk, kv_host ? 1 : 0, &p);
+  if (workspace_bytes < p.f_total)
+    return fail(UPIPE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes,
+                p.f_total);
+
+  std::lock_guard<std::mutex> lk(g_mu);
+  UPIPE_CUDA(cudaSetDevice(dev));
+  DevState* ds = nullptr;
+  st = dev_state(dev, &ds);
+  if (st != UPIPE_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* qw = ws + p.f_qw;
+  float* state_o = p.n_trunks > 1 ? reinterpret_cast<float*>(ws + p.f_state_o) : nullptr;
+  float* state_ml = p.n_trunks > 1 ? reinterpret_cast<float*>(ws + p.f_state_ml) : nullptr;
+  const float scale = 1.0f / std::sqrt(static_cast<float>(D));
+
+  Stager stg{p, ds, stream, k, v, {ws + p.f_slot_k[0], ws + p.f_slot_k[1]},
+             {ws + p.f_slot_v[0], ws + p.f_slot_v[1]}, {}, 0};
+  if (kv_host) {
+    for (int g = 0; g < Hq / p.hc; ++g)
+      for (int m = 0; m < p.n_trunks; ++m)
+        for (int n = 0; n <= (causal ? m : p.n_trunks - 1); ++n) stg.jobs.push_back({g * p.kc, n});
+    // The copy stream must not touch the workspace before earlier work on `stream` is done.
+    UPIPE_CUDA(cudaEventRecord(ds->entry, stream));
+    UPIPE_CUDA(cudaStreamWaitEvent(ds->copy, ds->entry, 0));
+  }
+  int job = 0;
+  for (int g = 0; g < Hq / p.hc; ++g) {
+    const int h0 = g * p.hc, kvh0 = g * p.kc;
+    UPIPE_CUDA(launch_seq_to_head(q, qw, B, S, Hq, D, h0, p.hc, stream));
+    if (!kv_host) {
+      UPIPE_CUDA(launch_seq_to_head(k, ws + p.f_kw, B, S, Hkv, D, kvh0, p.kc, stream));
+      UPIPE_CUDA(launch_seq_to_head(v, ws + p.f_vw, B, S, Hkv, D, kvh0, p.kc, stream));
+    }
+    CUtensorMap tq, tk, tv;
+    UPIPE_CUDA(make_tmap_bf16(&tq, qw, D, S, static_cast<int64_t>(B) * p.hc));
+    if (!kv_host) {
+      UPIPE_CUDA(make_tmap_bf16(&tk, ws + p.f_kw, D, S, static_cast<int64_t>(B) * p.kc));
+      UPIPE_CUDA(make_tmap_bf16(&tv, ws + p.f_vw, D, S, static_cast<int64_t>(B) * p.kc));
+    }
+    for (int m = 0; m < p.n_trunks; ++m) {
+      const int64_t q_lo = static_cast<int64_t>(m) * p.T;
+      const int64_t q_hi = std::min<int64_t>(S, q_lo + p.T);
+      const int n_last = causal ? m : p.n_trunks - 1;
+      for (int n = 0; n <= n_last; ++n, ++job) {
+        const int64_t t0 = static_cast<int64_t>(n) * p.T;
+        const int64_t Tn = std::min<int64_t>(p.T, S - t0);
+        FwdArgs a{};
+        a.q_lo = q_lo; a.q_hi = q_hi; a.S = S;
+        a.hc = p.hc; a.kc = p.kc; a.G = p.G; a.Hq = Hq; a.h0 = h0;
+        a.causal = causal; a.first = (n == 0); a.last = (n == n_last);
+        a.scale_log2 = scale * 1.4426950408889634f;
+        a.o = o; a.lse = lse;
+        a.state_o = state_o; a.state_ml = state_ml; a.state_rows = p.T_pad;
+        a.err = ds->err;
+        if (kv_host) {
+          st = stg.before(job);
+          if (st != UPIPE_OK) return st;
+          const int s = job & 1;
+          UPIPE_CUDA(make_tmap_bf16(&tk, stg.slot_k[s], D, Tn, static_cast<int64_t>(B) * p.kc));
+          UPIPE_CUDA(make_tmap_bf16(&tv, stg.slot_v[s], D, Tn, static_cast<int64_t>(B) * p.kc));
+          a.kv_row_lo = 0; a.kv_row_hi = Tn; a.kv_pos0 = t0;
+        } else {
+          a.kv_row_lo = t0; a.kv_row_hi = t0 + Tn; a.kv_pos0 = 0;
+        }
+        UPIPE_CUDA(launch_attn_fwd(D, B, tq, tk, tv, a, stream));
+        if (kv_host) {
+          st = stg.after(job);
+          if (st != UPIPE_OK) return st;
+        }
+      }
+    }
+  }
+  return UPIPE_OK;
+}
+
+int upipe_attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                   const void* dout, void* dq, void* dk, void* dv, int B, int64_t S, int Hq,
+                   int Hkv, int D, int causal, int head_chunk, int64_t seq_trunk,
+                   void* workspace, size_t workspace_bytes, void* stream_) {
+  g_last_error.clear();
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace)
+    return fail(UPIPE_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return fail(UPIPE_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(workspace) % kAlign)
+    return fail(UPIPE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  Plan p0;
+  int st = make_plan(B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk, 0, &p0);
+  if (st != UPIPE_OK) return st;
+  const void* dptrs[8] = {q, o, lse, dout, dq, dk, dv, workspace};
+  const char* names[8] = {"q", "o", "lse", "dout", "dq", "dk", "dv", "workspace"};
+  bool kv_host = false;
+  int dev = 0;
+  st = check_placement(dptrs, 8, names, k, v, &kv_host, &dev);
+  if (st != UPIPE_OK) return st;
+  Plan p;
+  make_plan(B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk, kv_host ? 1 : 0, &p);
+  if (workspace_bytes < p.b_total)
+    return fail(UPIPE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes,
+                p.b_total);
+
+  std::lock_guard<std::mutex> lk(g_mu);
+  UPIPE_CUDA(cudaSetDevice(dev));
+  DevState* ds = nullptr;
+  st = dev_state(dev, &ds);
+  if (st != UPIPE_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* qw = ws + p.b_qw;
+  void* dow = ws + p.b_dow;
+  float* dqacc = reinterpret_cast<float*>(ws + p.b_dqacc);
+  float* lse2 = reinterpret_cast<float*>(ws + p.b_lse2);
+  float* dvec = reinterpret_cast<float*>(ws + p.b_dvec);
+  const float scale = 1.0f / std::sqrt(static_cast<float>(D));
+
+  Stager stg{p, ds, stream, k, v, {ws + p.b_slot_k[0], ws + p.b_slot_k[1]},
+             {ws + p.b_slot_v[0], ws + p.b_slot_v[1]}, {}, 0};
+  if (kv_host) {
+    for (int g = 0; g < Hq / p.hc; ++g)
+      for (int n = 0; n < p.n_trunks; ++n) stg.jobs.push_back({g * p.kc, n});
+    UPIPE_CUDA(cudaEventRecord(ds->entry, stream));
+    UPIPE_CUDA(cudaStreamWaitEvent(ds->copy, ds->entry, 0));
+  }
+  int job = 0;
+  for (int g = 0; g < Hq / p.hc; ++g) {
+    const int h0 = g * p.hc, kvh0 = g * p.kc;
+    UPIPE_CUDA(launch_seq_to_head(q, qw, B, S, Hq, D, h0, p.hc, stream));
+    UPIPE_CUDA(launch_bwd_pre(o, dout, lse, dow, dvec, lse2, dqacc, B, S, p.S_pad, Hq, D, h0,
+                              p.hc, stream));
+    if (!kv_host) {
+      UPIPE_CUDA(launch_seq_to_head(k, ws + p.b_kw, B, S, Hkv, D, kvh0, p.kc, stream));
+      UPIPE_CUDA(launch_seq_to_head(v, ws + p.b_vw, B, S, Hkv, D, kvh0, p.kc, stream));
+    }
+    CUtensorMap tq, tdo, tk, tv;
+    UPIPE_CUDA(make_tmap_bf16(&tq, qw, D, S, static_cast<int64_t>(B) * p.hc));
+    UPIPE_CUDA(make_tmap_bf16(&tdo, dow, D, S, static_cast<int64_t>(B) * p.hc));
+    if (!kv_host) {
+      UPIPE_CUDA(make_tmap_bf16(&tk, ws + p.b_kw, D, S, static_cast<int64_t>(B) * p.kc));
+      UPIPE_CUDA(make_tmap_bf16(&tv, ws + p.b_vw, D, S, static_cast<int64_t>(B) * p.kc));
+    }
+    for (int n = 0; n < p.n_trunks; ++n, ++job) {
+      const int64_t t0 = static_cast<int64_t>(n) * p.T;
+      const int64_t Tn = std::min<int64_t>(p.T, S - t0);
+      BwdArgs a{};
+      a.S = S; a.S_pad = p.S_pad;
+      a.hc = p.hc; a.kc = p.kc; a.G = p.G; a.Hkv = Hkv; a.kvh0 = kvh0;
+      a.causal = causal; a.scale = scale; a.scale_log2 = scale * 1.4426950408889634f;
+      a.lse2 = lse2; a.dvec = dvec; a.dqacc = dqacc; a.dk = dk; a.dv = dv; a.err = ds->err;
+      if (kv_host) {
+        st = stg.before(job);
+        if (st != UPIPE_OK) return st;
+        const int s = job & 1;
+        UPIPE_CUDA(make_tmap_bf16(&tk, stg.slot_k[s], D, Tn, static_cast<int64_t>(B) * p.kc));
+        UPIPE_CUDA(make_tmap_bf16(&tv, stg.slot_v[s], D, Tn, static_cast<int64_t>(B) * p.kc));
+        a.kv_row_lo = 0; a.kv_row_hi = Tn; a.kv_pos0 = t0;
+      } else {
+        a.kv_row_lo = t0; a.kv_row_hi = t0 + Tn; a.kv_pos0 = 0;
+      }
+      UPIPE_CUDA(launch_attn_bwd(D, B, tq, tdo, tk, tv, a, stream));
+      if (kv_host) {
+        st = stg.after(job);
+        if (st != UPIPE_OK) return st;
+      }
+    }
+    UPIPE_CUDA(launch_dq_convert(dqacc, dq, B, S, p.S_pad, Hq, D, h0, p.hc, stream));
+  }
+  return UPIPE_OK;
+}
+
+static int layout_args(const void* src, const void* dst, int B, int64_t S, int H, int D,
+                       int h_begin, int h_count) {
+  if (!src || !dst) return fail(UPIPE_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(src) || !aligned16(dst))
+    return fail(UPIPE_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  if (B < 1 || S < 1 || H < 1 || D < 8 || D % 8)
+    return fail(UPIPE_ERR_INVALID_ARG, "bad sizes (B=%d S=%lld H=%d D=%d; D %% 8 == 0)", B,
+                static_cast<long long>(S), H, D);
+  if (h_begin < 0 || h_count < 1 || h_begin + h_count > H)
+    return fail(UPIPE_ERR_INVALID_ARG, "head range [%d, %d) outside [0, %d)", h_begin,
+                h_begin + h_count, H);
+  int d1 = -1, d2 = -1;
+  if (pointer_kind(src, &d1) != 0 || pointer_kind(dst, &d2) != 0 || d1 != d2)
+    return fail(UPIPE_ERR_INVALID_ARG, "src and dst must be memory of one device");
+  UPIPE_CUDA(cudaSetDevice(d1));
+  return UPIPE_OK;
+}
+
+int upipe_seq_to_head_major(const void* src, void* dst, int B, int64_t S, int H, int D,
+                            int h_begin, int h_count, void* stream) {
+  g_last_error.clear();
+  const int st = layout_args(src, dst, B, S, H, D, h_begin, h_count);
+  if (st != UPIPE_OK) return st;
+  UPIPE_CUDA(launch_seq_to_head(src, dst, B, S, H, D, h_begin, h_count,
+                                static_cast<cudaStream_t>(stream)));
+  return UPIPE_OK;
+}
+
+int upipe_head_to_seq_major(const void* src, void* dst, int B, int64_t S, int H, int D,
+                            int h_begin, int h_count, void* stream) {
+  g_last_error.clear();
+  const int st = layout_args(src, dst, B, S, H, D, h_begin, h_count);
+  if (st != UPIPE_OK) return st;
+  UPIPE_CUDA(launch_head_to_seq(src, dst, B, S, H, D, h_begin, h_count,
+                                static_cast<cudaStream_t>(stream)));
+  return UPIPE_OK;
+}
+
+int upipe_sync_status(void* stream) {
+  g_last_error.clear();
+  UPIPE_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+  int dev = 0;
+  UPIPE_CUDA(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (dev < 0 || dev >= kMaxDev || !g_dev[dev].ready) return UPIPE_OK;
+  uint32_t w = 0;
+  UPIPE_CUDA(cudaMemcpy(&w, g_dev[dev].err, sizeof(w), cudaMemcpyDeviceToHost));
+  if (w) {
+    UPIPE_CUDA(cudaMemset(g_dev[dev].err, 0, sizeof(w)));
+    return fail(UPIPE_ERR_TIMEOUT, "device status word 0x%x: a bounded wait expired", w);
+  }
+  return UPIPE_OK;
+}
+
+const char* upipe_status_string(int status) {
+  switch (status) {
+    case UPIPE_OK: return "UPIPE_OK";
+    case UPIPE_ERR_INVALID_ARG: return "UPIPE_ERR_INVALID_ARG";
+    case UPIPE_ERR_UNSUPPORTED: return "UPIPE_ERR_UNSUPPORTED";
+    case UPIPE_ERR_WORKSPACE_TOO_SMALL: return "UPIPE_ERR_WORKSPACE_TOO_SMALL";
+    case UPIPE_ERR_CUDA: return "UPIPE_ERR_CUDA";
+    case UPIPE_ERR_TIMEOUT: return "UPIPE_ERR_TIMEOUT";
+    default: return "UPIPE_ERR_UNKNOWN";
+  }
+}
+
+const char* upipe_last_error_message(void) { return g_last_error.c_str(); }
+
+void upipe_shutdown(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (int i = 0; i < kMaxDev; ++i) {
+    DevState& d = g_dev[i];
+    if (!d.ready) continue;
+    cudaSetDevice(i);
+    cudaStreamSynchronize(d.copy);
+    cudaStreamDestroy(d.copy);
+    for (int s = 0; s < 2; ++s) {
+      cudaEventDestroy(d.slot_ready[s]);
+      cudaEventDestroy(d.slot_free[s]);
+    }
+    cudaEventDestroy(d.entry);
+    cudaFree(d.err);
+    d = DevState{};
+  }
+}
+
+uint64_t upipe_launch_count(void) { return g_launches.load(); }
+
+int upipe_profile_enable(int on) {
+  g_profile.store(on != 0);
+  return UPIPE_OK;
+}
+
+int upipe_profile_read(upipe_kernel_stat* out, int n) {
+  g_last_error.clear();
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  for (const ProfRec& r : g_prof) {
+    float ms = 0.f;
+    cudaError_t e = cudaEventSynchronize(r.e1);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.e0, r.e1);
+    if (e != cudaSuccess) return cuda_fail(e, "profile event");
+    if (out && r.kclass >= 0 && r.kclass < n) {
+      out[r.kclass].total_ms += ms;
+      out[r.kclass].launches += 1;
+    }
+    g_event_pool.push_back(r.e0);
+    g_event_pool.push_back(r.e1);
+  }
+  g_prof.clear();
+  return UPIPE_OK;
+}
+
+int upipe_selftest_umma(const void* a, const void* b, float* c, int N, int K, int a_mn_major,
+                        int b_mn_major, int a_manual, int lbo, int sbo, void* stream) {
+  g_last_error.clear();
+  if (!a || !b || !c || !aligned16(a) || !aligned16(b) || !aligned16(c))
+    return fail(UPIPE_ERR_INVALID_ARG, "null or unaligned pointer");
+  if ((N != 64 && N != 128) || (K != 64 && K != 128))
+    return fail(UPIPE_ERR_INVALID_ARG, "N and K must be 64 or 128");
+  if (a_manual && a_mn_major) return fail(UPIPE_ERR_INVALID_ARG, "a_manual needs a K-major A");
+  if (lbo < 16 || lbo > 65536 || sbo < 16 || sbo > 65536 || lbo % 16 || sbo % 16)
+    return fail(UPIPE_ERR_INVALID_ARG, "lbo/sbo must be multiples of 16 in [16, 65536]");
+  // The descriptors may only address the two 32 KiB operand tiles.
+  if ((a_mn_major || b_mn_major) && 7 * 2048 + lbo + sbo + 1024 > 32768)
+    return fail(UPIPE_ERR_INVALID_ARG, "lbo/sbo would address outside the operand tile");
+  int dev = -1, d2 = -1, d3 = -1;
+  if (pointer_kind(a, &dev) != 0 || pointer_kind(b, &d2) != 0 || pointer_kind(c, &d3) != 0 ||
+      dev != d2 || dev != d3)
+    return fail(UPIPE_ERR_INVALID_ARG, "a, b, c must be memory of one device");
+  std::lock_guard<std::mutex> lk(g_mu);
+  UPIPE_CUDA(cudaSetDevice(dev));
+  DevState* ds = nullptr;
+  const int st = dev_state(dev, &ds);
+  if (st != UPIPE_OK) return st;
+  UPIPE_CUDA(launch_selftest_umma(a, b, c, N, K, a_mn_major, b_mn_major, a_manual, lbo, sbo,
+                                  ds->err, static_cast<cudaStream_t>(stream)));
+  return UPIPE_OK;
+}
+
+int upipe_selftest_wait_timeout(int limit_us, void* stream) {
+  g_last_error.clear();
+  if (limit_us < 1 || limit_us > 2000000)
+    return fail(UPIPE_ERR_INVALID_ARG, "limit_us must be in [1, 2000000]");
+  int dev = 0;
+  UPIPE_CUDA(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevState* ds = nullptr;
+  const int st = dev_state(dev, &ds);
+  if (st != UPIPE_OK) return st;
+  UPIPE_CUDA(launch_selftest_wait(limit_us, ds->err, static_cast<cudaStream_t>(stream)));
+  return UPIPE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,93 @@
+// Interface between the host-side scheduler (api.cpp) and the kernel translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace upipe {
+
+// ---- launch bookkeeping (api.cpp) ---------------------------------------------------------
+// Every kernel launch goes through begin/end so the library can count launches and, when
+// profiling is on, bracket each one with CUDA events on its own stream.
+void launch_begin(int kclass, cudaStream_t stream);
+void launch_end(int kclass, cudaStream_t stream);
+
+// Builds a 3-D bf16 tensor map over a dense [depth][rows][cols] array with a box of
+// 128 rows x 64 columns and 128-byte swizzle (cols % 64 == 0). Returns cudaSuccess or an
+// error if the driver refused the map.
+cudaError_t make_tmap_bf16(CUtensorMap* map, const void* base, int64_t cols, int64_t rows,
+                           int64_t depth);
+
+// ---- forward attention (attn_fwd.cu) -------------------------------------------------------
+struct FwdArgs {
+  int64_t q_lo, q_hi;            // global query rows covered by this launch (one Q trunk)
+  int64_t kv_row_lo, kv_row_hi;  // rows of the K/V map used by this launch (one KV trunk)
+  int64_t kv_pos0;               // global token position of K/V map row 0
+  int64_t S;                     // sequence length
+  int hc, kc, G, Hq, h0;         // group q-heads, group kv-heads, Hq/Hkv, total q-heads, first q-head
+  int causal, first, last;       // first: no carried state; last: finalise O and LSE
+  float scale_log2;              // softmax scale * log2(e)
+  void* o;                       // [B,S,Hq,D] bf16, written when last
+  float* lse;                    // [B,Hq,S], written when last
+  float* state_o;                // [B*hc][state_rows][D] fp32 running numerator (rows from q_lo)
+  float* state_ml;               // [B*hc][state_rows][2] fp32 running max (log2 units), sum
+  int64_t state_rows;
+  uint32_t* err;                 // device status word
+};
+
+// q_map: Q workspace [B*hc][S][D]; k_map / v_map: [B*kc][kv_rows][D].
+cudaError_t launch_attn_fwd(int D, int B, const CUtensorMap& q_map, const CUtensorMap& k_map,
+                            const CUtensorMap& v_map, const FwdArgs& a, cudaStream_t stream);
+
+// ---- backward attention (attn_bwd.cu) ------------------------------------------------------
+struct BwdArgs {
+  int64_t kv_row_lo, kv_row_hi;  // K/V map rows of this launch (one KV trunk)
+  int64_t kv_pos0;               // global token position of K/V map row 0
+  int64_t S, S_pad;              // sequence length, per-head row pitch of lse2/dvec/dqacc
+  int hc, kc, G, Hkv, kvh0;      // group sizes, total kv-heads, first kv-head of the group
+  int causal;
+  float scale, scale_log2;
+  const float* lse2;             // [B*hc][S_pad] LSE * log2(e)
+  const float* dvec;             // [B*hc][S_pad] D_i = <dO_i, O_i>
+  float* dqacc;                  // [B*hc][S_pad][D] fp32 dQ accumulator (scaled)
+  void* dk;                      // [B,S,Hkv,D] bf16
+  void* dv;                      // [B,S,Hkv,D] bf16
+  uint32_t* err;
+};
+
+// q_map / do_map: [B*hc][S][D]; k_map / v_map: [B*kc][kv_rows][D].
+cudaError_t launch_attn_bwd(int D, int B, const CUtensorMap& q_map, const CUtensorMap& do_map,
+                            const CUtensorMap& k_map, const CUtensorMap& v_map,
+                            const BwdArgs& a, cudaStream_t stream);
+
+// ---- HBM-bound helpers (layout.cu) ---------------------------------------------------------
+// dst[b][h][s][:] = src[b][s][h_begin + h][:]  for h < h_count   (bf16, D % 8 == 0)
+cudaError_t launch_seq_to_head(const void* src, void* dst, int B, int64_t S, int H, int D,
+                               int h_begin, int h_count, cudaStream_t stream);
+// dst[b][s][h_begin + h][:] = src[b][h][s][:]
+cudaError_t launch_head_to_seq(const void* src, void* dst, int B, int64_t S, int H, int D,
+                               int h_begin, int h_count, cudaStream_t stream);
+
+// Backward pre-pass for one head group (q-heads h0 .. h0+hc-1):
+//   dow[b*hc+h][s][:] = dout[b][s][h0+h][:]
+//   dvec[(b*hc+h)*S_pad + s] = sum_d dout*o   (fp32),  lse2[...] = lse[b][h0+h][s] * log2(e)
+//   dqacc[(b*hc+h)*S_pad + s][:] = 0
+// rows s in [S, S_pad) get dvec = lse2 = 0 and zeroed dqacc.
+cudaError_t launch_bwd_pre(const void* o, const void* dout, const float* lse, void* dow,
+                           float* dvec, float* lse2, float* dqacc, int B, int64_t S,
+                           int64_t S_pad, int Hq, int D, int h0, int hc, cudaStream_t stream);
+
+// dq[b][s][h0+h][:] = bf16(dqacc[(b*hc+h)*S_pad + s][:])
+cudaError_t launch_dq_convert(const float* dqacc, void* dq, int B, int64_t S, int64_t S_pad,
+                              int Hq, int D, int h0, int hc, cudaStream_t stream);
+
+// ---- self-tests (selftest.cu) --------------------------------------------------------------
+cudaError_t launch_selftest_umma(const void* a, const void* b, float* c, int N, int K,
+                                 int a_mn, int b_mn, int a_manual, int lbo, int sbo,
+                                 uint32_t* err, cudaStream_t stream);
+cudaError_t launch_selftest_wait(int limit_us, uint32_t* err, cudaStream_t stream);
+
+}  // namespace upipe

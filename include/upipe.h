@@ -1,0 +1,189 @@
+/*
+ * upipe.h - C ABI of a single-GPU (sm_103a) library for exact causal (GQA) self-attention,
+ * forward and backward, over very long sequences.
+ *
+ * The schedule follows two published designs:
+ *   - UPipe head chunking: attention heads are processed one group of `head_chunk` q-heads at
+ *     a time, every group reusing the same workspace ("Road to 5 million sequence length"
+ *     talk, UPipe passage; "Road to 5 Million Tokens" summary, section 2, item 6; UPipe
+ *     abstract, arXiv 2602.21196).
+ *   - FPDT sequence trunking: a query trunk folds key/value trunks 0..m into running
+ *     softmax statistics; key/value trunks may live in pinned host memory and are staged
+ *     into two device slots on a side copy stream while the previous trunk computes
+ *     ("Training Ultra Long Context LM with Fully Pipelined Distributed Transformer",
+ *     Key Findings items 1-3 and Technical Deep Dive).
+ *   - DeepSpeed Ulysses' head<->sequence all-to-all becomes, on one GPU, the
+ *     `upipe_seq_to_head_major` gather into the group workspace (FPDT talk, Technical Deep
+ *     Dive, first paragraph); the inverse scatter is fused into the kernels' epilogues.
+ *
+ * Definition computed (per batch b, q-head h, kv-head c = h / (Hq/Hkv), scale = 1/sqrt(D)):
+ *   s_ij = scale <q_i, k_j>, j <= i when causal;  P = row softmax(s);  O = P V;
+ *   LSE_i = ln sum_j exp(s_ij);  and the analytic gradients dQ, dK, dV of <dO, O>.
+ *
+ * Conventions shared by every entry point
+ *   - bf16 tensors are passed as `void*` / `const void*` to bf16 (IEEE bfloat16) data.
+ *   - Token-major layouts: q, o, dout, dq are [B, S, Hq, D]; k, v, dk, dv are [B, S, Hkv, D],
+ *     all dense row-major. lse is float32 [B, Hq, S], natural log.
+ *   - Every pointer must be 16-byte aligned. Device pointers must belong to the device that
+ *     is current for the caller; k and v may instead both be PINNED host memory
+ *     (cudaHostAlloc / cudaHostRegister), which selects the staged host-K/V path.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). All work is enqueued on it
+ *     and calls return before the GPU finishes (asynchronous, like a kernel launch).
+ *   - Ownership: the caller owns every buffer, including the workspace. Per call the library
+ *     allocates no device memory. Per device it lazily creates one internal copy stream,
+ *     a few events and a 256-byte device status word; upipe_shutdown() releases them.
+ *   - Errors: all arguments are validated before anything is enqueued; on an error nothing
+ *     is launched and a status code is returned (see upipe_status). A device-side bounded
+ *     wait that expires sets the device status word and the kernel exits early; the host
+ *     learns of it through upipe_sync_status(). Asynchronous CUDA faults surface at the
+ *     caller's next synchronisation.
+ */
+#ifndef UPIPE_H_
+#define UPIPE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  UPIPE_OK = 0,
+  UPIPE_ERR_INVALID_ARG = 1,          /* bad shape, pointer, alignment or placement */
+  UPIPE_ERR_UNSUPPORTED = 2,          /* valid request outside what the kernels implement */
+  UPIPE_ERR_WORKSPACE_TOO_SMALL = 3,  /* workspace_bytes < upipe_workspace_bytes(...) */
+  UPIPE_ERR_CUDA = 4,                 /* a CUDA runtime/driver call failed */
+  UPIPE_ERR_TIMEOUT = 5               /* a kernel's bounded wait expired (see sync_status) */
+} upipe_status;
+
+/* Which pass a workspace is sized for. */
+enum { UPIPE_PASS_FWD = 0, UPIPE_PASS_BWD = 1, UPIPE_PASS_BOTH = 2 };
+
+/*
+ * Bytes of device workspace one upipe_attn_fwd / upipe_attn_bwd call needs.
+ * Pure host arithmetic; touches no device. Returns 0 for arguments that the matching
+ * attention call would reject. Every term is proportional to head_chunk (q-heads) or to
+ * head_chunk/(Hq/Hkv) (kv-heads), so the workspace of a chunked call is head_chunk/Hq of the
+ * unchunked one at the same seq_trunk - the activation-memory cut UPipe reports (UPipe
+ * abstract, arXiv 2602.21196: up to 87.5% for a 32B model, i.e. 8 of 64 heads).
+ *   pass: UPIPE_PASS_FWD, UPIPE_PASS_BWD or UPIPE_PASS_BOTH (the max of the two).
+ *   kv_on_host: 1 if k/v will be pinned host memory (two trunk slots instead of full K/V).
+ */
+size_t upipe_workspace_bytes(int B, int64_t S, int Hq, int Hkv, int D, int causal,
+                             int head_chunk, int64_t seq_trunk, int pass, int kv_on_host);
+
+/*
+ * Forward: o = softmax(scale q k^T + mask) v, lse = ln(sum exp(...)).
+ *   q [B,S,Hq,D] bf16 (device); k, v [B,S,Hkv,D] bf16 (device, or both pinned host);
+ *   o [B,S,Hq,D] bf16 (device, written); lse [B,Hq,S] float32 (device, written).
+ *   causal: 1 = key j visible to query i iff j <= i; 0 = full attention.
+ *   head_chunk: q-heads per group; must divide Hq and be a multiple of Hq/Hkv (a group owns
+ *     whole kv-heads). head_chunk = Hq is the unchunked schedule.
+ *   seq_trunk: trunk length T in tokens. T >= S means one trunk; otherwise T % 128 == 0.
+ *     The last trunk may be shorter (ragged).
+ *   workspace: device buffer of >= upipe_workspace_bytes(..., UPIPE_PASS_FWD, kv_on_host)
+ *     bytes, 256-byte aligned; contents on entry are ignored and on exit are undefined.
+ *   Supported: D in {64, 128}; any S >= 1; B, Hq, Hkv >= 1 (UNSUPPORTED otherwise).
+ */
+int upipe_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                   int B, int64_t S, int Hq, int Hkv, int D, int causal, int head_chunk,
+                   int64_t seq_trunk, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Backward: given the forward's o and lse and the upstream gradient dout, writes
+ * dq [B,S,Hq,D], dk and dv [B,S,Hkv,D] (bf16, device; fully overwritten).
+ * P is recomputed from lse (no S x S tensor is stored), D_i = <dout_i, o_i> is formed by a
+ * pre-kernel, dq accumulates in a float32 workspace buffer and is converted at the end.
+ * Same argument rules as upipe_attn_fwd; workspace sized with UPIPE_PASS_BWD.
+ */
+int upipe_attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                   const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                   int B, int64_t S, int Hq, int Hkv, int D, int causal, int head_chunk,
+                   int64_t seq_trunk, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Layout transforms standing in for the Ulysses all-to-all on one GPU (HBM-bound copies).
+ *   seq_to_head_major: src token-major [B,S,H,D] -> dst head-major [B,h_count,S,D] holding
+ *     heads [h_begin, h_begin+h_count).
+ *   head_to_seq_major: the inverse; writes only those heads of dst [B,S,H,D].
+ * bf16, device pointers, 16-byte aligned; D must be a multiple of 8.
+ */
+int upipe_seq_to_head_major(const void* src, void* dst, int B, int64_t S, int H, int D,
+                            int h_begin, int h_count, void* stream);
+int upipe_head_to_seq_major(const void* src, void* dst, int B, int64_t S, int H, int D,
+                            int h_begin, int h_count, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status word.
+ * Returns UPIPE_OK, UPIPE_ERR_TIMEOUT (a kernel's bounded wait expired since the last
+ * check) or UPIPE_ERR_CUDA (the synchronisation itself failed).
+ */
+int upipe_sync_status(void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* upipe_status_string(int status);
+
+/* Detail of the last error on the calling thread ("" if none). Valid until the next call. */
+const char* upipe_last_error_message(void);
+
+/* Releases the per-device copy streams, events and status words. Optional at exit. */
+void upipe_shutdown(void);
+
+/* ---- Diagnostics ---------------------------------------------------------------------- */
+
+/* Kernel classes for launch counting and profiling. */
+enum {
+  UPIPE_K_LAYOUT = 0,     /* seq_to_head_major / head_to_seq_major gathers */
+  UPIPE_K_ATTN_FWD = 1,   /* forward attention kernel */
+  UPIPE_K_BWD_PRE = 2,    /* D = rowsum(dO * O) + dO gather + LSE prescale */
+  UPIPE_K_ATTN_BWD = 3,   /* backward attention kernel */
+  UPIPE_K_DQ_CONVERT = 4, /* dq float32 -> bf16 token-major */
+  UPIPE_K_OTHER = 5,      /* self-tests */
+  UPIPE_K_COUNT = 6
+};
+
+typedef struct {
+  double total_ms;   /* summed CUDA-event time of the recorded launches */
+  uint64_t launches; /* launches recorded */
+} upipe_kernel_stat;
+
+/* Total kernel launches made by this library in this process (all classes). */
+uint64_t upipe_launch_count(void);
+
+/*
+ * Profiling: while enabled, every launch is bracketed by CUDA events recorded on the stream
+ * it is launched on. upipe_profile_read() synchronises those events, adds their elapsed
+ * times into out[0..n) (indexed by kernel class) and forgets them. Returns a status code.
+ */
+int upipe_profile_enable(int on);
+int upipe_profile_read(upipe_kernel_stat* out, int n);
+
+/*
+ * Self-test of the tensor-core tile path: one 128 x N x K bf16 MMA tile (fp32 accumulate)
+ * computed with the same TMA loads, shared-memory descriptors and TMEM read-back the
+ * attention kernels use. c[m][n] = sum_k A(m,k) B(n,k) with
+ *   a_mn_major = 0: a is [128][K] row-major;  1: a is [K][128] row-major;
+ *   b_mn_major = 0: b is [N][K] row-major;    1: b is [K][N] row-major;
+ *   a_manual = 1 stores A into shared memory with the kernels' own swizzled stores instead
+ *     of TMA (a_mn_major must be 0).
+ * N, K in {64, 128}. lbo/sbo: byte offsets written into the MN-major descriptors.
+ * c is float32 [128][N]. Device pointers. Test use only.
+ */
+int upipe_selftest_umma(const void* a, const void* b, float* c, int N, int K,
+                        int a_mn_major, int b_mn_major, int a_manual, int lbo, int sbo,
+                        void* stream);
+
+/*
+ * Self-test of the bounded device wait: launches one CTA that waits on a shared-memory
+ * barrier that nothing completes, with a limit of `limit_us` microseconds (1..2000000).
+ * The kernel gives up, sets the status word and returns; a following
+ * upipe_sync_status(stream) must report UPIPE_ERR_TIMEOUT.
+ */
+int upipe_selftest_wait_timeout(int limit_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* UPIPE_H_ */

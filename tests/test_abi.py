@@ -1,0 +1,149 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports every function the
+header declares, sizes workspaces by the documented formula, and rejects bad arguments before
+touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import context_parallelism_gb300 as up
+from workloads import WORKLOADS, WORKLOAD_ORDER
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "upipe.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(upipe_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("upipe_attn_fwd", "upipe_attn_bwd", "upipe_workspace_bytes",
+                 "upipe_seq_to_head_major", "upipe_head_to_seq_major", "upipe_sync_status"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(up.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in upipe.h but not exported"
+    assert set(declared_functions()) == set(up.SIGNATURES), "binding and header disagree"
+
+
+def _expected_ws(B, S, Hq, Hkv, D, hc, T, kv_host):
+    """The workspace arena as documented: every segment 256-byte aligned."""
+    al = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    G = Hq // Hkv
+    kc = hc // G
+    T = min(T, S)
+    S_pad = (S + 127) // 128 * 128
+    T_pad = (T + 127) // 128 * 128
+    ntr = (S + T - 1) // T
+    qw = B * hc * S * D * 2
+    kv = 4 * al(B * kc * T * D * 2) if kv_host else 2 * al(B * kc * S * D * 2)
+    fwd = al(qw) + kv
+    if ntr > 1:
+        fwd += al(B * hc * T_pad * D * 4) + al(B * hc * T_pad * 8)
+    bwd = 2 * al(qw) + kv + al(B * hc * S_pad * D * 4) + 2 * al(B * hc * S_pad * 4)
+    return fwd, bwd
+
+
+@pytest.mark.parametrize("name", WORKLOAD_ORDER)
+def test_workspace_matches_formula(name):
+    w = WORKLOADS[name]
+    fwd, bwd = _expected_ws(w.B, w.S, w.Hq, w.Hkv, w.D, w.head_chunk, w.seq_trunk, w.kv_on_host)
+    args = (w.B, w.S, w.Hq, w.Hkv, w.D, 1, w.head_chunk, w.seq_trunk)
+    assert up.upipe_workspace_bytes(*args, up.UPIPE_PASS_FWD, w.kv_on_host) == fwd
+    assert up.upipe_workspace_bytes(*args, up.UPIPE_PASS_BWD, w.kv_on_host) == bwd
+    assert up.upipe_workspace_bytes(*args, up.UPIPE_PASS_BOTH, w.kv_on_host) == max(fwd, bwd)
+
+
+@pytest.mark.parametrize("name", WORKLOAD_ORDER)
+@pytest.mark.parametrize("pass_", [0, 1])
+def test_workspace_scales_with_head_chunk(name, pass_):
+    """Chunked / unchunked workspace = head_chunk / Hq at the same trunk: the 32B-class
+    workload with 8 of 64 heads per group is the 87.5% cut the UPipe abstract reports."""
+    w = WORKLOADS[name]
+    G = w.Hq // w.Hkv
+    full = up.upipe_workspace_bytes(w.B, w.S, w.Hq, w.Hkv, w.D, 1, w.Hq, w.seq_trunk, pass_,
+                                    w.kv_on_host)
+    for hc in range(G, w.Hq + 1, G):
+        if w.Hq % hc:
+            continue
+        part = up.upipe_workspace_bytes(w.B, w.S, w.Hq, w.Hkv, w.D, 1, hc, w.seq_trunk, pass_,
+                                        w.kv_on_host)
+        assert part * w.Hq <= full * hc + 256 * 16 * w.Hq
+        assert abs(part / full - hc / w.Hq) < 1e-6
+    if name == "gqa32b_s256k_peaky":
+        part = up.upipe_workspace_bytes(w.B, w.S, w.Hq, w.Hkv, w.D, 1, 8, w.seq_trunk, pass_, 0)
+        full = up.upipe_workspace_bytes(w.B, w.S, w.Hq, w.Hkv, w.D, 1, 64, w.seq_trunk, pass_, 0)
+        assert part / full == pytest.approx(0.125, abs=1e-9)
+
+
+@pytest.mark.parametrize("args", [
+    (0, 512, 4, 4, 64, 1, 4, 512),      # B = 0
+    (1, 0, 4, 4, 64, 1, 4, 512),        # S = 0
+    (1, 512, 6, 4, 64, 1, 6, 512),      # Hq % Hkv
+    (1, 512, 32, 8, 128, 1, 6, 512),    # head_chunk does not divide Hq
+    (1, 512, 32, 8, 128, 1, 2, 512),    # head_chunk not a multiple of Hq/Hkv
+    (1, 1024, 4, 4, 64, 1, 4, 300),     # seq_trunk < S and not a multiple of 128
+    (1, 512, 4, 4, 64, 2, 4, 512),      # causal not 0/1
+])
+def test_workspace_zero_for_invalid(args):
+    assert up.upipe_workspace_bytes(*args, 0, 0) == 0
+
+
+FAKE = 1 << 20  # an aligned non-null address; validation must fail before it is dereferenced
+
+
+@pytest.mark.parametrize("args,status", [
+    ((1, 512, 6, 4, 64, 1, 6, 512), up.UPIPE_ERR_INVALID_ARG),
+    ((1, 512, 32, 8, 128, 1, 2, 512), up.UPIPE_ERR_INVALID_ARG),
+    ((1, 1024, 4, 4, 64, 1, 4, 300), up.UPIPE_ERR_INVALID_ARG),
+    ((1, 512, 4, 4, 96, 1, 4, 512), up.UPIPE_ERR_UNSUPPORTED),
+    ((1, 512, 4, 4, 256, 1, 4, 512), up.UPIPE_ERR_UNSUPPORTED),
+])
+def test_attention_calls_validate_before_device_access(args, status):
+    B, S, Hq, Hkv, D, causal, hc, T = args
+    st = up._lib.upipe_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, B, S, Hq, Hkv, D, causal, hc, T,
+                                FAKE, 1 << 40, None)
+    assert st == status, up.upipe_last_error_message()
+    assert up.upipe_last_error_message()
+    st = up._lib.upipe_attn_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, B, S, Hq,
+                                Hkv, D, causal, hc, T, FAKE, 1 << 40, None)
+    assert st == status
+
+
+def test_null_and_misaligned_pointers_rejected():
+    st = up._lib.upipe_attn_fwd(None, FAKE, FAKE, FAKE, FAKE, 1, 512, 4, 4, 64, 1, 4, 512, FAKE,
+                                1 << 30, None)
+    assert st == up.UPIPE_ERR_INVALID_ARG
+    st = up._lib.upipe_attn_fwd(FAKE + 2, FAKE, FAKE, FAKE, FAKE, 1, 512, 4, 4, 64, 1, 4, 512,
+                                FAKE, 1 << 30, None)
+    assert st == up.UPIPE_ERR_INVALID_ARG
+    st = up._lib.upipe_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 512, 4, 4, 64, 1, 4, 512,
+                                FAKE + 16, 1 << 30, None)
+    assert st == up.UPIPE_ERR_INVALID_ARG  # workspace must be 256-byte aligned
+    st = up._lib.upipe_seq_to_head_major(FAKE, FAKE, 1, 16, 4, 64, 3, 2, None)
+    assert st == up.UPIPE_ERR_INVALID_ARG  # head range outside H
+    st = up._lib.upipe_seq_to_head_major(FAKE, FAKE, 1, 16, 4, 60, 0, 2, None)
+    assert st == up.UPIPE_ERR_INVALID_ARG  # D % 8
+    st = up._lib.upipe_selftest_wait_timeout(0, None)
+    assert st == up.UPIPE_ERR_INVALID_ARG
+
+
+def test_status_strings():
+    for s in range(6):
+        assert up.upipe_status_string(s).startswith("UPIPE_")
+    assert up.upipe_status_string(99) == "UPIPE_ERR_UNKNOWN"
+
+
+def test_launch_count_and_profile_read_without_gpu():
+    assert up.upipe_launch_count() >= 0
+    up.upipe_profile_enable(False)
+    stats = up.upipe_profile_read()
+    assert set(stats) == set(up.KERNEL_CLASSES)

@@ -1,0 +1,149 @@
+"""Element-by-element parity of the CUDA forward and backward (through the C ABI) with the fp64
+oracle, on inputs small enough for the oracle to run in full: the two small workloads, ragged
+sequence lengths, several trunks, non-causal attention, GQA ratios, and K/V staged from
+pinned host memory. Needs an sm_103a GPU."""
+import pytest
+import torch
+
+import context_parallelism_gb300 as up
+import oracle
+from tests._parity import check_full, gpu_fwd_bwd, pinned_copy
+from workloads import WORKLOADS, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle(q, k, v, do, causal):
+    o, lse, dq, dk, dv = oracle.attn_bwd_ref(q, k, v, do, causal=causal)
+    return o, lse, dq, dk, dv
+
+
+@pytest.mark.parametrize("name", ["mha_s512_d64", "llama8b_s8k"])
+def test_small_workloads_full(name):
+    w = WORKLOADS[name]
+    q, k, v, do = make_inputs(w)  # CPU, seeded
+    ref = _oracle(q, k, v, do, w.causal)
+    qg, kg, vg, dog = (t.cuda() for t in (q, k, v, do))
+    gpu = gpu_fwd_bwd(qg, kg, vg, dog, w.causal, w.head_chunk, w.seq_trunk)
+    check_full(gpu, ref, name)
+
+
+CASES = [
+    # B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk, kv_on_host
+    (2, 1000, 8, 2, 128, True, 4, 256, False),   # ragged S, 4 trunks (last ragged), 2 groups
+    (2, 1000, 8, 2, 128, True, 8, 1000, False),  # ragged S, one trunk, one group
+    (1, 1000, 8, 2, 128, False, 4, 384, False),  # non-causal, ragged trunks
+    (2, 777, 4, 4, 64, True, 2, 256, False),     # D = 64, MHA, ragged
+    (1, 1000, 8, 2, 128, True, 4, 256, True),    # K/V in pinned host memory, double buffer
+    (1, 640, 8, 1, 128, True, 8, 128, True),     # G = 8, many small host trunks
+    (1, 129, 4, 2, 64, True, 2, 128, False),     # one full tile + 1-row tail
+    (1, 1, 2, 1, 128, True, 2, 1, False),        # a single token
+    (3, 300, 6, 3, 128, False, 6, 300, False),   # odd head counts, non-causal
+]
+
+
+@pytest.mark.parametrize("B,S,Hq,Hkv,D,causal,hc,T,kv_host", CASES)
+def test_parity_cases(B, S, Hq, Hkv, D, causal, hc, T, kv_host):
+    w = WORKLOADS["llama8b_s8k"].with_(B=B, S=S, Hq=Hq, Hkv=Hkv, D=D, causal=causal,
+                                       seed=7 + S + Hq)
+    q, k, v, do = make_inputs(w, "cpu")
+    ref = _oracle(q, k, v, do, causal)
+    qg, dog = q.cuda(), do.cuda()
+    if kv_host:
+        kg, vg = pinned_copy(k), pinned_copy(v)
+    else:
+        kg, vg = k.cuda(), v.cuda()
+    gpu = gpu_fwd_bwd(qg, kg, vg, dog, causal, hc, T)
+    check_full(gpu, ref, f"{B}x{S}x{Hq}/{Hkv}x{D} causal={causal} hc={hc} T={T} host={kv_host}")
+
+
+def test_head_chunk_does_not_change_forward_bits():
+    """Grouping heads changes memory, not the per-head computation: O and LSE are bitwise
+    identical for every head_chunk at a fixed trunk length."""
+    w = WORKLOADS["llama8b_s8k"].with_(S=2048, seed=31)
+    q, k, v, _ = (t.cuda() for t in make_inputs(w, "cpu"))
+    outs = []
+    for hc in (4, 8, 16, 32):
+        o, lse = up.attention_forward(q, k, v, causal=True, head_chunk=hc, seq_trunk=2048)
+        up.upipe_sync_status()
+        outs.append((o, lse))
+    for o, lse in outs[1:]:
+        assert torch.equal(o, outs[0][0])
+        assert torch.equal(lse, outs[0][1])
+
+
+def test_trunk_length_sweep_matches_oracle():
+    """Q trunk m folding KV trunks 0..m over several launches gives the untrunked result."""
+    w = WORKLOADS["llama8b_s8k"].with_(S=2048, seed=32)
+    q, k, v, do = make_inputs(w, "cpu")
+    ref = _oracle(q, k, v, do, True)
+    qg, kg, vg, dog = (t.cuda() for t in (q, k, v, do))
+    for T in (256, 512, 1024, 2048):
+        gpu = gpu_fwd_bwd(qg, kg, vg, dog, True, 8, T)
+        check_full(gpu, ref, f"T={T}")
+
+
+def test_host_kv_equals_device_kv_forward():
+    """Staging K/V trunks from pinned host memory changes where bytes come from, not the
+    arithmetic: the forward is bitwise identical to the device-resident run."""
+    w = WORKLOADS["llama8b_s8k"].with_(S=1536, seed=33)
+    q, k, v, _ = make_inputs(w, "cpu")
+    qg = q.cuda()
+    o1, l1 = up.attention_forward(qg, k.cuda(), v.cuda(), causal=True, head_chunk=8, seq_trunk=512)
+    o2, l2 = up.attention_forward(qg, pinned_copy(k), pinned_copy(v), causal=True, head_chunk=8,
+                                  seq_trunk=512)
+    up.upipe_sync_status()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_forward_is_deterministic():
+    w = WORKLOADS["llama8b_s8k"].with_(S=1024, seed=34)
+    q, k, v, _ = (t.cuda() for t in make_inputs(w, "cpu"))
+    a = up.attention_forward(q, k, v, head_chunk=8, seq_trunk=512)
+    b = up.attention_forward(q, k, v, head_chunk=8, seq_trunk=512)
+    up.upipe_sync_status()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_pageable_host_kv_rejected_without_launch():
+    w = WORKLOADS["mha_s512_d64"]
+    q, k, v, _ = make_inputs(w, "cpu")
+    n0 = up.upipe_launch_count()
+    with pytest.raises(up.UpipeError) as ei:
+        up.attention_forward(q.cuda(), k, v)  # pageable CPU tensors
+    assert ei.value.status == up.UPIPE_ERR_INVALID_ARG
+    assert up.upipe_launch_count() == n0
+
+
+def test_workspace_too_small_rejected():
+    w = WORKLOADS["mha_s512_d64"]
+    q, k, v, _ = (t.cuda() for t in make_inputs(w, "cpu"))
+    need = up.upipe_workspace_bytes(1, 512, 4, 4, 64, 1, 4, 512, up.UPIPE_PASS_FWD, 0)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty((1, 4, 512), device="cuda")
+    with pytest.raises(up.UpipeError) as ei:
+        up.upipe_attn_fwd(q, k, v, o, lse, 1, 512, 4, 4, 64, 1, 4, 512, ws, need - 256)
+    assert ei.value.status == up.UPIPE_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_no_device_allocation_per_call():
+    """The caller's workspace is the only device memory a call uses: torch's allocator and the
+    device's free memory are unchanged across calls after the first."""
+    w = WORKLOADS["llama8b_s8k"].with_(S=1024, seed=35)
+    q, k, v, do = (t.cuda() for t in make_inputs(w, "cpu"))
+    gpu_fwd_bwd(q, k, v, do, True, 8, 512)  # first call creates the per-device state
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    o = torch.empty_like(q)
+    lse = torch.empty((1, 32, 1024), device="cuda")
+    need = up.upipe_workspace_bytes(1, 1024, 32, 8, 128, 1, 8, 512, up.UPIPE_PASS_FWD, 0)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        up.upipe_attn_fwd(q, k, v, o, lse, 1, 1024, 32, 8, 128, 1, 8, 512, ws)
+    up.upipe_sync_status()
+    free2, _ = torch.cuda.mem_get_info()
+    assert free2 == free1
+    assert free0 - free1 <= o.nbytes + lse.nbytes + ws.nbytes + (64 << 20)
