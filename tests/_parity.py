@@ -18,9 +18,13 @@ GRAD_REL_FRO = 2e-2
 
 
 def rel_fro(x, ref):
+    """||x - ref||_F / ||ref||_F. Where the exact gradient vanishes identically (one token:
+    P = 1 so dS = 0 and dQ = dK = 0), the denominator is floored at an RMS of 1e-3 per
+    element so that rounding noise of the order of fp32 ulps is not divided by zero."""
     x = np.asarray(x, np.float64)
     ref = np.asarray(ref, np.float64)
-    return float(np.linalg.norm(x - ref) / max(np.linalg.norm(ref), 1e-30))
+    floor = 1e-3 * np.sqrt(max(ref.size, 1))
+    return float(np.linalg.norm(x - ref) / max(np.linalg.norm(ref), floor))
 
 
 def max_abs(x, ref):
