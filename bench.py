@@ -42,6 +42,8 @@ def _args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--seq-len", type=int, default=None,
+                    help="override S (small profiling captures only; not a bench line)")
     return ap.parse_args()
 
 
@@ -182,6 +184,9 @@ def run_ours(a):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = WORKLOADS[a.workload]
+    if a.seq_len:
+        w = w.with_(S=a.seq_len, seq_trunk=min(w.seq_trunk, a.seq_len),
+                    name=f"{w.name}@S={a.seq_len}")
     hc = a.head_chunk or w.head_chunk
     T = a.seq_trunk or w.seq_trunk
     kv_host = w.kv_on_host

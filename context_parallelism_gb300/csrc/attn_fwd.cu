@@ -272,12 +272,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       l_sum *= alpha;
       const float mb = (m_used == -INFINITY) ? 0.f : m_used;
+      // P is rounded to bf16 here, once; the row sum adds exactly the rounded weights the
+      // P.V MMA consumes, so O stays a convex combination of V rows (a dominant weight's
+      // rounding cancels) and LSE moves by at most one bf16 rounding (2^-9 relative).
+      uint32_t pk[64];
       float sum = 0.f;
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const float p = ex2_approx(fmaf(sv[c], a.scale_log2, -mb));
-        sv[c] = p;
-        sum += p;
+      for (int c = 0; c < 128; c += 2) {
+        const uint32_t w = pack_bf16(ex2_approx(fmaf(sv[c], a.scale_log2, -mb)),
+                                     ex2_approx(fmaf(sv[c + 1], a.scale_log2, -mb)));
+        pk[c >> 1] = w;
+        sum += __uint_as_float(w << 16) + __uint_as_float(w & 0xFFFF0000u);
       }
       l_sum += sum;
 
@@ -300,12 +305,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
       }
 #pragma unroll
-      for (int cc = 0; cc < 16; ++cc) {
-        st_shared_v4(sP + swz_offset(t, cc * 8), pack_bf16(sv[cc * 8 + 0], sv[cc * 8 + 1]),
-                     pack_bf16(sv[cc * 8 + 2], sv[cc * 8 + 3]),
-                     pack_bf16(sv[cc * 8 + 4], sv[cc * 8 + 5]),
-                     pack_bf16(sv[cc * 8 + 6], sv[cc * 8 + 7]));
-      }
+      for (int cc = 0; cc < 16; ++cc)
+        st_shared_v4(sP + swz_offset(t, cc * 8), pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2],
+                     pk[4 * cc + 3]);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(B.p_full);
