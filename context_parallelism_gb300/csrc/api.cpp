@@ -676,6 +676,7 @@ int upipe_selftest_umma(const void* a, const void* b, float* c, int N, int K, in
     return fail(UPIPE_ERR_INVALID_ARG, "null or unaligned pointer");
   if ((N != 64 && N != 128) || (K != 64 && K != 128))
     return fail(UPIPE_ERR_INVALID_ARG, "N and K must be 64 or 128");
+  if (a_manual < 0 || a_manual > 2) return fail(UPIPE_ERR_INVALID_ARG, "a_manual must be 0, 1 or 2");
   if (a_manual && a_mn_major) return fail(UPIPE_ERR_INVALID_ARG, "a_manual needs a K-major A");
   if (lbo < 16 || lbo > 65536 || sbo < 16 || sbo > 65536 || lbo % 16 || sbo % 16)
     return fail(UPIPE_ERR_INVALID_ARG, "lbo/sbo must be multiples of 16 in [16, 65536]");

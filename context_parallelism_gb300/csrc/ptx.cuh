@@ -137,6 +137,19 @@ __device__ __forceinline__ void umma_f16_ss(uint32_t d_tmem, uint64_t adesc, uin
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f16. A (M = 128 rows) sits in TMEM with row m
+// in lane m and its bf16 elements packed two per 32-bit column, so a 16-element reduction step
+// spans 8 columns.
+__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrives once on `bar` when every tcgen05 async operation issued so far by this thread is done.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile(
@@ -221,8 +234,9 @@ constexpr uint32_t kBoxBytes = 128 * 128;  // one 128-row x 64-element bf16 box
 // K-major operand (the reduction dimension is contiguous in a row): the k-th group of 16
 // reduction elements starts 32 bytes further inside a box, and a new box every 64 elements.
 // Rows advance in 8-row groups of 1024 bytes (stride byte offset).
-__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile_saddr, int k16) {
-  const uint32_t a = tile_saddr + static_cast<uint32_t>(k16 >> 2) * kBoxBytes +
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile_saddr, int k16,
+                                                uint32_t box_bytes = kBoxBytes) {
+  const uint32_t a = tile_saddr + static_cast<uint32_t>(k16 >> 2) * box_bytes +
                      static_cast<uint32_t>(k16 & 3) * 32u;
   return sdesc(a, 16u, 1024u);
 }
@@ -257,6 +271,12 @@ __device__ __forceinline__ uint32_t swz_offset(int r, int col) {
 }
 
 // ---- small numeric helpers ----------------------------------------------------------------
+// Fire-and-forget fp32 add to global memory (no return value, relaxed, GPU scope).
+__device__ __forceinline__ void red_add_f32(float* addr, float v) {
+  asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+}
+
+
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

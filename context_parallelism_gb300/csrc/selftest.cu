@@ -38,7 +38,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
     fence_mbar_init();
   }
   if (warp == 0) {
-    tmem_alloc(slot, 128);
+    tmem_alloc(slot, 256);  // accumulator at column 0, a TMEM-resident A at column 128
     tmem_relinquish();
   }
   tc_fence_before();
@@ -48,7 +48,20 @@ __global__ void __launch_bounds__(kStThreads, 1)
   uint8_t* sA = smem + StSmemLayout::kA;
   uint8_t* sB = smem + StSmemLayout::kB;
 
-  if (a_manual) {
+  if (a_manual == 2) {
+    // Row t of A into TMEM lane t, two bf16 per 32-bit column (the MMA's TMEM A layout).
+    uint32_t r[32];
+    for (int half = 0; half < 2; ++half) {
+      for (int i = 0; i < 32; ++i) {
+        const uint32_t lo = reinterpret_cast<const uint16_t*>(a_raw)[t * 128 + half * 64 + 2 * i];
+        const uint32_t hi = reinterpret_cast<const uint16_t*>(a_raw)[t * 128 + half * 64 + 2 * i + 1];
+        r[i] = lo | (hi << 16);
+      }
+      tmem_st32(tmem + 128 + (static_cast<uint32_t>(warp * 32) << 16) + half * 32, r);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+  } else if (a_manual) {
     // Row t of A ([128][128] row-major) into the swizzled K-major image.
     for (int col = 0; col < 128; col += 8) {
       const uint4 v = *reinterpret_cast<const uint4*>(a_raw + static_cast<size_t>(t) * 128 + col);
@@ -70,11 +83,15 @@ __global__ void __launch_bounds__(kStThreads, 1)
       tc_fence_after();
       const uint32_t idesc = idesc_bf16(128, N, a_mn != 0, b_mn != 0);
       for (int k16 = 0; k16 < K / 16; ++k16) {
-        const uint64_t da = a_mn ? desc_mnmajor(smem_u32(sA), k16, lbo, sbo)
-                                 : desc_kmajor(smem_u32(sA), k16);
         const uint64_t db = b_mn ? desc_mnmajor(smem_u32(sB), k16, lbo, sbo)
                                  : desc_kmajor(smem_u32(sB), k16);
-        umma_f16_ss(tmem, da, db, idesc, k16 > 0);
+        if (a_manual == 2) {
+          umma_f16_ts(tmem, tmem + 128 + k16 * 8, db, idesc, k16 > 0);
+        } else {
+          const uint64_t da = a_mn ? desc_mnmajor(smem_u32(sA), k16, lbo, sbo)
+                                   : desc_kmajor(smem_u32(sA), k16);
+          umma_f16_ss(tmem, da, db, idesc, k16 > 0);
+        }
       }
       umma_commit(bar_mma);
       ok = mbar_wait(bar_mma, 0);
@@ -93,7 +110,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 128);
+    tmem_dealloc(tmem, 256);
   }
 }
 

@@ -166,7 +166,8 @@ int upipe_profile_read(upipe_kernel_stat* out, int n);
  *   a_mn_major = 0: a is [128][K] row-major;  1: a is [K][128] row-major;
  *   b_mn_major = 0: b is [N][K] row-major;    1: b is [K][N] row-major;
  *   a_manual = 1 stores A into shared memory with the kernels' own swizzled stores instead
- *     of TMA (a_mn_major must be 0).
+ *     of TMA; a_manual = 2 stores A into tensor memory (row m in lane m, two bf16 per
+ *     column) and issues the MMA with A read from there (a_mn_major must be 0 for both).
  * N, K in {64, 128}. lbo/sbo: byte offsets written into the MN-major descriptors.
  * c is float32 [128][N]. Device pointers. Test use only.
  */

@@ -22,6 +22,8 @@ LAYOUTS = [  # (a_mn, b_mn, a_manual): the combinations the forward and backward
     (0, 0, 1),
     (1, 1, 0),  # dQ = dS K (A = dS^T tile read MN-major)
     (1, 0, 0),
+    (0, 1, 2),  # A from tensor memory (P kept in TMEM), B MN-major
+    (0, 0, 2),
 ]
 
 
