@@ -42,6 +42,8 @@ SIGNATURES = {
                             _sz, _vp]),
     "upipe_attn_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i64, _i, _i, _i,
                             _i, _i, _i64, _vp, _sz, _vp]),
+    "upipe_attn_fwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i64, _i, _i, _i, _i, _i, _i64,
+                                    _i, _vp]),
     "upipe_seq_to_head_major": (_i, [_vp, _vp, _i, _i64, _i, _i, _i, _i, _vp]),
     "upipe_head_to_seq_major": (_i, [_vp, _vp, _i, _i64, _i, _i, _i, _i, _vp]),
     "upipe_sync_status": (_i, [_vp]),
@@ -129,6 +131,15 @@ def upipe_attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, S, Hq, Hkv, D, causal, 
                              _ptr(dk), _ptr(dv), B, S, Hq, Hkv, D, int(causal), head_chunk,
                              seq_trunk, _ptr(workspace), wb, _stream(stream, q, dq))
     _check(st, "upipe_attn_bwd")
+
+
+def upipe_attn_fwd_noalloc(q, k, v, o, lse, B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk,
+                           check_status=0, stream=None):
+    """The forward with its scratch in the library's static device array (no allocation)."""
+    st = _lib.upipe_attn_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, S, Hq, Hkv,
+                                     D, int(causal), head_chunk, seq_trunk, int(check_status),
+                                     _stream(stream, q, o))
+    _check(st, "upipe_attn_fwd_noalloc")
 
 
 def upipe_seq_to_head_major(src, dst, B, S, H, D, h_begin, h_count, stream=None):

@@ -112,6 +112,8 @@ cudaEvent_t pool_event() {
 
 }  // namespace
 
+void set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
+
 void launch_begin(int kclass, cudaStream_t stream) {
   (void)kclass;
   g_launches.fetch_add(1, std::memory_order_relaxed);

@@ -15,6 +15,9 @@ namespace upipe {
 void launch_begin(int kclass, cudaStream_t stream);
 void launch_end(int kclass, cudaStream_t stream);
 
+// Records the message upipe_last_error_message() returns on this thread.
+void set_last_error(const char* msg);
+
 // Builds a 3-D bf16 tensor map over a dense [depth][rows][cols] array with a box of
 // 128 rows x 64 columns and 128-byte swizzle (cols % 64 == 0). Returns cudaSuccess or an
 // error if the driver refused the map.

@@ -103,6 +103,31 @@ int upipe_attn_bwd(const void* q, const void* k, const void* v, const void* o,
                    int64_t seq_trunk, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * upipe_attn_fwd without a caller-supplied workspace, for callers that cannot allocate device
+ * memory (code running under an allocator or memory pool that owns every device byte, real-time
+ * code that forbids allocation after start-up, plugins handed only their inputs and outputs).
+ * The pages describe no such call; it has no counterpart there.
+ *   - The forward's scratch is a file-scope static device array of 32 MiB, created when the
+ *     library's device code is loaded on a GPU and held by every GPU that loads it until the
+ *     process exits. Problems whose forward workspace (upipe_workspace_bytes, UPIPE_PASS_FWD,
+ *     kv_on_host = 0) exceeds 32 MiB are rejected with UPIPE_ERR_WORKSPACE_TOO_SMALL; e.g. the
+ *     Llama3-8B-shaped layer fits up to S = 8192 with head_chunk = 8.
+ *   - No call allocates or frees anything (no cudaMalloc/cudaFree, no allocating library call).
+ *   - The first call on a device does the per-device set-up (looks up the array's device
+ *     address and clears its status word, a synchronous step); make that first call before any
+ *     stream capture.
+ *   - Every call shares the one array, which keeps the last call's contents. Calls whose GPU
+ *     work overlaps (different streams, or unordered host threads) race on it: serialise them.
+ *   - Arguments as upipe_attn_fwd, except that k and v must be device memory and there is no
+ *     workspace. check_status != 0 first synchronises `stream` and returns UPIPE_ERR_TIMEOUT if
+ *     a kernel of an earlier call of this function gave up on a bounded wait (blocking; pass 0
+ *     to enqueue without waiting).
+ */
+int upipe_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int64_t S, int Hq, int Hkv, int D, int causal, int head_chunk,
+                           int64_t seq_trunk, int check_status, void* stream);
+
+/*
  * Layout transforms standing in for the Ulysses all-to-all on one GPU (HBM-bound copies).
  *   seq_to_head_major: src token-major [B,S,H,D] -> dst head-major [B,h_count,S,D] holding
  *     heads [h_begin, h_begin+h_count).
