@@ -44,6 +44,10 @@ def _args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--seq-len", type=int, default=None,
                     help="override S (small profiling captures only; not a bench line)")
+    ap.add_argument("--sweep", default=None, choices=["chunk-trunk", "host-kv"],
+                    help="print one JSON line per sweep point instead of the bench line: "
+                         "chunk-trunk = head_chunk x seq_trunk grid; host-kv = the same "
+                         "workload with K/V on the device and in pinned host memory")
     return ap.parse_args()
 
 
@@ -130,6 +134,27 @@ def oracle_sample(w, S_sample, inputs=None):
     desc = (f"fp64 numpy oracle fwd+bwd on the first {S_sample} of {w.S} tokens, all {w.Hq} "
             f"q-heads ({src}); FLOPs by the same causal convention")
     return flops / dt / 1e12, dt, flops, desc, cores
+
+
+def job_throughput(local_ms, steps, flops_per_step, world, reduce_max=None):
+    """Whole-job TFLOP/s of N independent replicas: every rank ran `steps` steps of
+    `flops_per_step`; the job takes as long as its slowest rank. Returns (tflops, max_ms)."""
+    t_max = float(local_ms)
+    if reduce_max is not None:
+        t_max = float(reduce_max(t_max))
+    return world * flops_per_step * steps / (t_max / 1e3) / 1e12, t_max
+
+
+def torch_reduce_max(device):
+    """MAX all-reduce of one float over the default process group (NCCL or gloo)."""
+    import torch
+    import torch.distributed as dist
+
+    def f(x):
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+    return f
 
 
 def _dist():
@@ -256,14 +281,10 @@ def run_ours(a):
     for e0, e1, e2 in ev:
         fwd_ms += e0.elapsed_time(e1)
         bwd_ms += e1.elapsed_time(e2)
-    t_max = elapsed
-    if world > 1:
-        tt = torch.tensor([elapsed], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_max = float(tt.item())
-    ms_per_step = t_max / a.steps
     f_fwd, f_bwd = w.flops_fwd(), w.flops_bwd()
-    value = world * (f_fwd + f_bwd) * a.steps / (t_max / 1e3) / 1e12
+    red = torch_reduce_max(dev) if world > 1 else None
+    value, t_max = job_throughput(elapsed, a.steps, f_fwd + f_bwd, world, red)
+    ms_per_step = t_max / a.steps
     peaks, peak_src = _peaks()
     peak = float(peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"])
 
@@ -338,13 +359,8 @@ def run_ours(a):
             e2e_step()
         e1.record(stream)
         barrier()
-        te = e0.elapsed_time(e1)
-        if world > 1:
-            tt = torch.tensor([te], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            te = float(tt.item())
-        line["e2e"] = {"value": world * (f_fwd + f_bwd) * a.steps / (te / 1e3) / 1e12,
-                       "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+        e2e_value, _ = job_throughput(e0.elapsed_time(e1), a.steps, f_fwd + f_bwd, world, red)
+        line["e2e"] = {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                        "d2h_bytes_per_step": int(d2h)}
         up.upipe_sync_status(stream)
 
@@ -359,8 +375,80 @@ def run_ours(a):
         print(json.dumps(line), flush=True)
 
 
+def run_sweep(a):
+    """Forward + backward TFLOP/s and workspace over a grid of schedules (one GPU)."""
+    import torch
+
+    import context_parallelism_gb300 as up
+    from workloads import WORKLOADS, make_inputs
+
+    w = WORKLOADS[a.workload]
+    if a.seq_len:
+        w = w.with_(S=a.seq_len, seq_trunk=min(w.seq_trunk, a.seq_len))
+    dev = torch.device("cuda", 0)
+    q, k, v, do = (t.to(dev) for t in make_inputs(w, "cuda" if w.gen_device == "cuda" else "cpu"))
+    if a.sweep == "chunk-trunk":
+        grid = sorted({(hc, T) for hc in (4, 8, 16, 32) if hc % w.G == 0 and w.Hq % hc == 0
+                       for T in (16384, 32768, w.S) if T <= w.S})
+        kv_modes = [False]
+    else:
+        grid = [(a.head_chunk or w.head_chunk, a.seq_trunk or w.seq_trunk)]
+        kv_modes = [False, True]
+    for kv_host in kv_modes:
+        if kv_host:
+            kk = torch.empty(k.shape, dtype=k.dtype, pin_memory=True)
+            kk.copy_(k)
+            vv = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+            vv.copy_(v)
+        else:
+            kk, vv = k, v
+        for hc, T in grid:
+            ws_b = up.upipe_workspace_bytes(w.B, w.S, w.Hq, w.Hkv, w.D, 1, hc, T,
+                                            up.UPIPE_PASS_BOTH, kv_host)
+            ws = torch.empty(ws_b, dtype=torch.uint8, device=dev)
+            o = torch.empty_like(q)
+            lse = torch.empty((w.B, w.Hq, w.S), dtype=torch.float32, device=dev)
+            dq = torch.empty_like(q)
+            dk = torch.empty_like(k)
+            dv = torch.empty_like(v)
+            args = (w.B, w.S, w.Hq, w.Hkv, w.D, 1, hc, T)
+
+            def fwd():
+                up.upipe_attn_fwd(q, kk, vv, o, lse, *args, ws, ws_b)
+
+            def bwd():
+                up.upipe_attn_bwd(q, kk, vv, o, lse, do, dq, dk, dv, *args, ws, ws_b)
+
+            for _ in range(max(1, a.warmup)):
+                fwd()
+                bwd()
+            torch.cuda.synchronize()
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            tf = tb = 0.0
+            for _ in range(a.steps):
+                e[0].record()
+                fwd()
+                e[1].record()
+                bwd()
+                e[2].record()
+                torch.cuda.synchronize()
+                tf += e[0].elapsed_time(e[1])
+                tb += e[1].elapsed_time(e[2])
+            up.upipe_sync_status()
+            ff, fb = w.flops_fwd() * a.steps, w.flops_bwd() * a.steps
+            print(json.dumps({
+                "sweep": a.sweep, "workload": w.name, "S": w.S, "head_chunk": hc,
+                "seq_trunk": T, "kv_on_host": kv_host, "fwd_tflops": ff / tf / 1e9,
+                "bwd_tflops": fb / tb / 1e9, "fwdbwd_tflops": (ff + fb) / (tf + tb) / 1e9,
+                "ms_per_step": (tf + tb) / a.steps, "workspace_gb": ws_b / 1e9}), flush=True)
+            del ws
+
+
 def main():
     a = _args()
+    if a.sweep:
+        run_sweep(a)
+        return
     if a.impl == "reference":
         run_reference(a)
     else:

@@ -140,7 +140,7 @@ std::once_flag g_encode_once;
 }  // namespace
 
 cudaError_t make_tmap_bf16(CUtensorMap* map, const void* base, int64_t cols, int64_t rows,
-                           int64_t depth) {
+                           int64_t depth, int box_rows) {
   std::call_once(g_encode_once, [] {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -154,7 +154,7 @@ cudaError_t make_tmap_bf16(CUtensorMap* map, const void* base, int64_t cols, int
                               static_cast<cuuint64_t>(depth)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols * 2),
                                  static_cast<cuuint64_t>(cols * rows * 2)};
-  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -518,14 +518,14 @@ int upipe_attn_bwd(const void* q, const void* k, const void* v, const void* o, c
     const int h0 = g * p.hc, kvh0 = g * p.kc;
     UPIPE_CUDA(launch_seq_to_head(q, qw, B, S, Hq, D, h0, p.hc, stream));
     UPIPE_CUDA(launch_bwd_pre(o, dout, lse, dow, dvec, lse2, dqacc, B, S, p.S_pad, Hq, D, h0,
-                              p.hc, stream));
+                              p.hc, scale, stream));
     if (!kv_host) {
       UPIPE_CUDA(launch_seq_to_head(k, ws + p.b_kw, B, S, Hkv, D, kvh0, p.kc, stream));
       UPIPE_CUDA(launch_seq_to_head(v, ws + p.b_vw, B, S, Hkv, D, kvh0, p.kc, stream));
     }
     CUtensorMap tq, tdo, tk, tv;
-    UPIPE_CUDA(make_tmap_bf16(&tq, qw, D, S, static_cast<int64_t>(B) * p.hc));
-    UPIPE_CUDA(make_tmap_bf16(&tdo, dow, D, S, static_cast<int64_t>(B) * p.hc));
+    UPIPE_CUDA(make_tmap_bf16(&tq, qw, D, S, static_cast<int64_t>(B) * p.hc, bwd_q_box_rows(D)));
+    UPIPE_CUDA(make_tmap_bf16(&tdo, dow, D, S, static_cast<int64_t>(B) * p.hc, bwd_q_box_rows(D)));
     if (!kv_host) {
       UPIPE_CUDA(make_tmap_bf16(&tk, ws + p.b_kw, D, S, static_cast<int64_t>(B) * p.kc));
       UPIPE_CUDA(make_tmap_bf16(&tv, ws + p.b_vw, D, S, static_cast<int64_t>(B) * p.kc));

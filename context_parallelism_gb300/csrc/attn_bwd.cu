@@ -1,4 +1,5 @@
-// Backward causal (GQA) attention on sm_103a.
+// Backward causal (GQA) attention on sm_103a, one 128-row query tile per step (used for
+// D = 64; D = 128 runs the ping-pong kernel in attn_bwd_pp.cu).
 //
 // One CTA owns a 128-row key/value tile of one kv-head and walks the query tiles of every
 // q-head of its group that can see it (query rows >= the tile's first key when causal). Per
@@ -12,11 +13,12 @@
 //   S^T  = K Q^T                (tcgen05, TMEM cols [0,128))
 //   dP^T = V dO^T               (tcgen05, TMEM cols [128,256))
 //   P^T  = exp2(S^T * scale*log2e - LSE_i*log2e), masked   (registers -> smem, bf16)
-//   dS^T = P^T * (dP^T - D_i)                             (registers -> smem, bf16)
+//   dS^T = P^T * (scale*dP^T - scale*D_i)                 (registers -> smem, bf16)
 //   dV  += P^T dO               (tcgen05, TMEM cols [256,256+D))
-//   dK  += dS^T Q               (tcgen05, TMEM cols [256+D,256+2D)), scaled at the end
-//   dQ   = dS K                 (tcgen05, TMEM cols [0,D), reusing S^T), scaled and added to
-//                               the fp32 dQ accumulator with vector atomics
+//   dK  += dS^T Q               (tcgen05, TMEM cols [256+D,256+2D))
+//   dQ   = dS K                 (tcgen05, TMEM cols [0,D), reusing S^T), added to the fp32
+//                               dQ accumulator with vector atomics
+// (the softmax scale rides in dS, so dK and dQ need no scaling afterwards)
 //
 // CTA layout (192 threads): warps 0-3 compute (thread t = key row t), warp 4 TMEM + MMA
 // issue, warp 5 TMA producer. Shared memory: K, V (resident), Q, dO (one stage), P^T, dS^T,
@@ -241,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool vis = key_ok && (i < a.S) && (!a.causal || i >= pj);
           const float pv = vis ? ex2_approx(fmaf(__uint_as_float(rs[x]), a.scale_log2, -lse_s[col])) : 0.f;
           p[x] = pv;
-          ds[x] = pv * (__uint_as_float(rd[x]) - dv_s[col]);
+          ds[x] = pv * fmaf(__uint_as_float(rd[x]), a.scale, -dv_s[col]);
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -272,9 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int x = 0; x < 32; x += 4)
             atomicAdd(reinterpret_cast<float4*>(dqrow + c * 32 + x),
-                      make_float4(__uint_as_float(r[x]) * a.scale, __uint_as_float(r[x + 1]) * a.scale,
-                                  __uint_as_float(r[x + 2]) * a.scale,
-                                  __uint_as_float(r[x + 3]) * a.scale));
+                      make_float4(__uint_as_float(r[x]), __uint_as_float(r[x + 1]),
+                                  __uint_as_float(r[x + 2]), __uint_as_float(r[x + 3])));
         }
       }
       tc_fence_before();
@@ -316,8 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          w[i] = pack_bf16(__uint_as_float(r[2 * i]) * a.scale,
-                           __uint_as_float(r[2 * i + 1]) * a.scale);
+          w[i] = pack_bf16(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
         if (store) {
 #pragma unroll
           for (int i = 0; i < 4; ++i)
@@ -360,9 +360,10 @@ cudaError_t launch_impl(int B, const CUtensorMap& q_map, const CUtensorMap& do_m
 
 }  // namespace
 
-cudaError_t launch_attn_bwd(int D, int B, const CUtensorMap& q_map, const CUtensorMap& do_map,
-                            const CUtensorMap& k_map, const CUtensorMap& v_map,
-                            const BwdArgs& a, cudaStream_t stream) {
+cudaError_t launch_attn_bwd_generic(int D, int B, const CUtensorMap& q_map,
+                                    const CUtensorMap& do_map, const CUtensorMap& k_map,
+                                    const CUtensorMap& v_map, const BwdArgs& a,
+                                    cudaStream_t stream) {
   if (D == 128) return launch_impl<128>(B, q_map, do_map, k_map, v_map, a, stream);
   if (D == 64) return launch_impl<64>(B, q_map, do_map, k_map, v_map, a, stream);
   return cudaErrorInvalidValue;

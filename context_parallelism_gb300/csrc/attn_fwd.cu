@@ -1,4 +1,5 @@
-// Forward causal (GQA) attention on sm_103a: TMA-staged Q/K/V tiles, tcgen05 MMAs with TMEM
+// Forward causal (GQA) attention on sm_103a, one 128-row query tile per CTA (used for D = 64;
+// D = 128 runs the two-tile ping-pong kernel in attn_fwd_pp.cu): TMA-staged Q/K/V tiles, tcgen05 MMAs with TMEM
 // accumulators for S = Q K^T and O += P V, online softmax in registers (one query row per
 // thread), causal tile skipping, and optional carried state so that a query trunk can fold
 // key/value trunks in over several launches.
@@ -389,8 +390,9 @@ cudaError_t launch_impl(int B, const CUtensorMap& q_map, const CUtensorMap& k_ma
 
 }  // namespace
 
-cudaError_t launch_attn_fwd(int D, int B, const CUtensorMap& q_map, const CUtensorMap& k_map,
-                            const CUtensorMap& v_map, const FwdArgs& a, cudaStream_t stream) {
+cudaError_t launch_attn_fwd_generic(int D, int B, const CUtensorMap& q_map,
+                                    const CUtensorMap& k_map, const CUtensorMap& v_map,
+                                    const FwdArgs& a, cudaStream_t stream) {
   if (D == 128) return launch_impl<128>(B, q_map, k_map, v_map, a, stream);
   if (D == 64) return launch_impl<64>(B, q_map, k_map, v_map, a, stream);
   return cudaErrorInvalidValue;

@@ -19,10 +19,10 @@ void launch_end(int kclass, cudaStream_t stream);
 void set_last_error(const char* msg);
 
 // Builds a 3-D bf16 tensor map over a dense [depth][rows][cols] array with a box of
-// 128 rows x 64 columns and 128-byte swizzle (cols % 64 == 0). Returns cudaSuccess or an
+// box_rows rows x 64 columns and 128-byte swizzle (cols % 64 == 0). Returns cudaSuccess or an
 // error if the driver refused the map.
 cudaError_t make_tmap_bf16(CUtensorMap* map, const void* base, int64_t cols, int64_t rows,
-                           int64_t depth);
+                           int64_t depth, int box_rows = 128);
 
 // ---- forward attention (attn_fwd.cu) -------------------------------------------------------
 struct FwdArgs {
@@ -42,6 +42,9 @@ struct FwdArgs {
 };
 
 // q_map: Q workspace [B*hc][S][D]; k_map / v_map: [B*kc][kv_rows][D].
+cudaError_t launch_attn_fwd_generic(int D, int B, const CUtensorMap& q_map,
+                                    const CUtensorMap& k_map, const CUtensorMap& v_map,
+                                    const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_attn_fwd(int D, int B, const CUtensorMap& q_map, const CUtensorMap& k_map,
                             const CUtensorMap& v_map, const FwdArgs& a, cudaStream_t stream);
 
@@ -54,14 +57,20 @@ struct BwdArgs {
   int causal;
   float scale, scale_log2;
   const float* lse2;             // [B*hc][S_pad] LSE * log2(e)
-  const float* dvec;             // [B*hc][S_pad] D_i = <dO_i, O_i>
-  float* dqacc;                  // [B*hc][S_pad][D] fp32 dQ accumulator (scaled)
+  const float* dvec;             // [B*hc][S_pad] scale * D_i,  D_i = <dO_i, O_i>
+  float* dqacc;                  // [B*hc][S_pad][D] fp32 dQ accumulator
   void* dk;                      // [B,S,Hkv,D] bf16
   void* dv;                      // [B,S,Hkv,D] bf16
   uint32_t* err;
 };
 
-// q_map / do_map: [B*hc][S][D]; k_map / v_map: [B*kc][kv_rows][D].
+// q_map / do_map: [B*hc][S][D] with boxes of bwd_q_box_rows(D) rows; k_map / v_map:
+// [B*kc][kv_rows][D] with 128-row boxes.
+int bwd_q_box_rows(int D);
+cudaError_t launch_attn_bwd_generic(int D, int B, const CUtensorMap& q_map,
+                                    const CUtensorMap& do_map, const CUtensorMap& k_map,
+                                    const CUtensorMap& v_map, const BwdArgs& a,
+                                    cudaStream_t stream);
 cudaError_t launch_attn_bwd(int D, int B, const CUtensorMap& q_map, const CUtensorMap& do_map,
                             const CUtensorMap& k_map, const CUtensorMap& v_map,
                             const BwdArgs& a, cudaStream_t stream);
@@ -76,12 +85,13 @@ cudaError_t launch_head_to_seq(const void* src, void* dst, int B, int64_t S, int
 
 // Backward pre-pass for one head group (q-heads h0 .. h0+hc-1):
 //   dow[b*hc+h][s][:] = dout[b][s][h0+h][:]
-//   dvec[(b*hc+h)*S_pad + s] = sum_d dout*o   (fp32),  lse2[...] = lse[b][h0+h][s] * log2(e)
+//   dvec[(b*hc+h)*S_pad + s] = scale * sum_d dout*o (fp32), lse2[...] = lse[b][h0+h][s]*log2(e)
 //   dqacc[(b*hc+h)*S_pad + s][:] = 0
 // rows s in [S, S_pad) get dvec = lse2 = 0 and zeroed dqacc.
 cudaError_t launch_bwd_pre(const void* o, const void* dout, const float* lse, void* dow,
                            float* dvec, float* lse2, float* dqacc, int B, int64_t S,
-                           int64_t S_pad, int Hq, int D, int h0, int hc, cudaStream_t stream);
+                           int64_t S_pad, int Hq, int D, int h0, int hc, float scale,
+                           cudaStream_t stream);
 
 // dq[b][s][h0+h][:] = bf16(dqacc[(b*hc+h)*S_pad + s][:])
 cudaError_t launch_dq_convert(const float* dqacc, void* dq, int B, int64_t S, int64_t S_pad,

@@ -4,7 +4,7 @@
 //     ("Training Ultra Long Context LM with Fully Pipelined Distributed Transformer",
 //     Technical Deep Dive, first paragraph). Here it copies one head group of a token-major
 //     [B,S,H,D] tensor into a head-major [B,h,S,D] workspace (and back).
-//   * the backward pre-pass: D_i = <dO_i, O_i> in fp32, the dO gather, the LSE prescale by
+//   * the backward pre-pass: scale * D_i, D_i = <dO_i, O_i> in fp32, the dO gather, the LSE prescale by
 //     log2(e) and the zeroing of the fp32 dQ accumulator, fused in one pass;
 //   * the dQ conversion: fp32 accumulator -> bf16 token-major dq.
 // Each thread moves 16-byte vectors; grids are sized as a multiple of the SM count and loop.
@@ -70,7 +70,7 @@ __global__ void bwd_pre_kernel(const uint4* __restrict__ o, const uint4* __restr
                                const float* __restrict__ lse, uint4* __restrict__ dow,
                                float* __restrict__ dvec, float* __restrict__ lse2,
                                float4* __restrict__ dqacc, int B, int64_t S, int64_t S_pad, int Hq,
-                               int Dc, int h0, int hc) {
+                               int Dc, int h0, int hc, float scale) {
   const int64_t rows = static_cast<int64_t>(B) * S_pad * hc;
   const int64_t total = rows * Dc;
   const float kLog2e = 1.4426950408889634f;
@@ -108,7 +108,7 @@ __global__ void bwd_pre_kernel(const uint4* __restrict__ o, const uint4* __restr
     }
     for (int off = Dc / 2; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
     if (live && c == 0) {
-      dvec[zrow] = (s < S) ? dot : 0.f;
+      dvec[zrow] = (s < S) ? dot * scale : 0.f;
       lse2[zrow] = (s < S) ? lse[(b * Hq + h0 + h) * S + s] * kLog2e : 0.f;
     }
   }
@@ -162,14 +162,15 @@ cudaError_t launch_head_to_seq(const void* src, void* dst, int B, int64_t S, int
 
 cudaError_t launch_bwd_pre(const void* o, const void* dout, const float* lse, void* dow,
                            float* dvec, float* lse2, float* dqacc, int B, int64_t S,
-                           int64_t S_pad, int Hq, int D, int h0, int hc, cudaStream_t stream) {
+                           int64_t S_pad, int Hq, int D, int h0, int hc, float scale,
+                           cudaStream_t stream) {
   const int Dc = D / 8;
   const int64_t work = static_cast<int64_t>(B) * S_pad * hc * Dc;
   launch_begin(2, stream);
   bwd_pre_kernel<<<grid_for(work, kLayoutThreads), kLayoutThreads, 0, stream>>>(
       static_cast<const uint4*>(o), static_cast<const uint4*>(dout), lse,
       static_cast<uint4*>(dow), dvec, lse2, reinterpret_cast<float4*>(dqacc), B, S, S_pad, Hq, Dc,
-      h0, hc);
+      h0, hc, scale);
   cudaError_t e = cudaGetLastError();
   launch_end(2, stream);
   return e;
