@@ -216,6 +216,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
 
+      // Issue order S(it), dV/dK/dQ(it-1), dP(it): five MMA blocks separate dQ(it-2) from
+      // dP(it), which reuses its TMEM columns, so the read-out of dQ hides behind them; the
+      // group's P(it) overlaps dV/dK/dQ(it-1) and its dS(it) overlaps S(it+1).
       for (int it = 0; ok && it < n_it; ++it) {
         const int st = it % kStages, w = it & 1, j = it >> 1;
         const uint32_t tS = tmem + 256 + 128 * w, tDP = tS + 64;
@@ -230,6 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_f16_ss(tS, desc_kmajor(sK, k16), desc_kmajor(sQ, k16, kQBox), id_sdp,
                       k16 > 0 ? 1u : 0u);
         umma_commit(s_full + w);
+        if (it >= 1 && !finish(it - 1)) { ok = false; break; }
         // dP[w] last held dQ^T of subtile it-2 until the group read it out.
         if (j >= 1 && !wait(dq_free + w, (j - 1) & 1)) { ok = false; break; }
         tc_fence_after();
@@ -238,7 +242,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_f16_ss(tDP, desc_kmajor(sV, k16), desc_kmajor(sDO, k16, kQBox), id_sdp,
                       k16 > 0 ? 1u : 0u);
         umma_commit(dp_full + w);
-        if (it >= 1) ok = finish(it - 1);
       }
       if (ok && n_it > 0) ok = finish(n_it - 1);
       if (ok) {
@@ -277,13 +280,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         uint32_t r[64];
         tmem_ld64_sync(tS + lane_off, r);
+        const uint64_t sl2 = f2_pack(a.scale_log2, a.scale_log2);
 #pragma unroll
         for (int x = 0; x < 64; x += 4) {
           const float4 l4 = *reinterpret_cast<const float4*>(lse_s + x);
-          p[x + 0] = ex2_approx(fmaf(__uint_as_float(r[x + 0]), a.scale_log2, -l4.x));
-          p[x + 1] = ex2_approx(fmaf(__uint_as_float(r[x + 1]), a.scale_log2, -l4.y));
-          p[x + 2] = ex2_approx(fmaf(__uint_as_float(r[x + 2]), a.scale_log2, -l4.z));
-          p[x + 3] = ex2_approx(fmaf(__uint_as_float(r[x + 3]), a.scale_log2, -l4.w));
+          float y0, y1, y2, y3;
+          f2_unpack(ffma2(f2_pack_u(r[x], r[x + 1]), sl2, f2_pack(-l4.x, -l4.y)), y0, y1);
+          f2_unpack(ffma2(f2_pack_u(r[x + 2], r[x + 3]), sl2, f2_pack(-l4.z, -l4.w)), y2, y3);
+          p[x + 0] = ex2_approx(y0);
+          p[x + 1] = ex2_approx(y1);
+          p[x + 2] = ex2_approx(y2);
+          p[x + 3] = ex2_approx(y3);
         }
       }
       if (need_mask) {
@@ -313,11 +320,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float4 db = *reinterpret_cast<const float4*>(dv_s + u * 8 + 4);
           const float dvv[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
           uint32_t pk[4];
+          const uint64_t sc2 = f2_pack(a.scale, a.scale);
 #pragma unroll
           for (int x = 0; x < 4; ++x) {
             const int col = u * 8 + 2 * x;
-            const float d0 = p[col] * fmaf(__uint_as_float(r[col]), a.scale, -dvv[2 * x]);
-            const float d1 = p[col + 1] * fmaf(__uint_as_float(r[col + 1]), a.scale, -dvv[2 * x + 1]);
+            const uint64_t t2 = ffma2(f2_pack_u(r[col], r[col + 1]), sc2,
+                                      f2_pack(-dvv[2 * x], -dvv[2 * x + 1]));
+            float d0, d1;
+            f2_unpack(fmul2(t2, f2_pack(p[col], p[col + 1])), d0, d1);
             pk[x] = pack_bf16(d0, d1);
           }
           st_shared_v4(sDS + swz_offset(t, u * 8), pk[0], pk[1], pk[2], pk[3]);

@@ -243,15 +243,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (a.causal) lim = min(lim, qrow - p0 + 1);
       }
       // Pass 1 over S (TMEM): the row maximum. Keeping the row in TMEM and reading it twice
-      // keeps the softmax within the 168 registers a 10-warp CTA allows.
+      // keeps the softmax within the 168 registers a 10-warp CTA allows. Only tiles that
+      // straddle the diagonal or an end pay for the mask.
       float mx = -INFINITY;
+      if (need_mask) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32_sync(tS + lane_off + c * 32, r);
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld32_sync(tS + lane_off + c * 32, r);
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          mx = fmaxf(mx, (c * 32 + i < lim) ? __uint_as_float(r[i]) : -INFINITY);
+          for (int i = 0; i < 32; i += 2)
+            mx = fmax3(mx, (c * 32 + i < lim) ? __uint_as_float(r[i]) : -INFINITY,
+                       (c * 32 + i + 1 < lim) ? __uint_as_float(r[i + 1]) : -INFINITY);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld32_sync(tS + lane_off + c * 32, r);
+#pragma unroll
+          for (int i = 0; i < 32; i += 2)
+            mx = fmax3(mx, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+        }
       }
       const float m_new = fmaxf(m_used, mx * a.scale_log2);
       float alpha = 1.f;
@@ -275,26 +288,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float mb = (m_used == -INFINITY) ? 0.f : m_used;
       // Pass 2: P rounded to bf16 once, written over S's first 64 columns; the row sum adds
-      // exactly the weights the P.V MMA consumes. Columns 64..127 are read before any P lands
-      // there (P of columns c..c+31 goes to column c/2..).
-      float sum = 0.f;
+      // exactly the weights the P.V MMA consumes (paired fp32 adds of the two bf16 halves).
+      // Columns 64..127 are read before any P lands there (P of columns c..c+31 goes to
+      // columns c/2..c/2+15).
+      const uint64_t sl2 = f2_pack(a.scale_log2, a.scale_log2);
+      const uint64_t nm2 = f2_pack(-mb, -mb);
+      uint64_t sum2 = f2_pack(0.f, 0.f);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
         tmem_ld32_sync(tS + lane_off + c * 32, r);
+        if (need_mask) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (c * 32 + i >= lim) r[i] = __float_as_uint(-INFINITY);
+        }
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const int col = c * 32 + 2 * i;
-          const float s0 = (col < lim) ? __uint_as_float(r[2 * i]) : -INFINITY;
-          const float s1 = (col + 1 < lim) ? __uint_as_float(r[2 * i + 1]) : -INFINITY;
-          const uint32_t v = pack_bf16(ex2_approx(fmaf(s0, a.scale_log2, -mb)),
-                                       ex2_approx(fmaf(s1, a.scale_log2, -mb)));
+          float x0, x1;
+          f2_unpack(ffma2(f2_pack_u(r[2 * i], r[2 * i + 1]), sl2, nm2), x0, x1);
+          const uint32_t v = pack_bf16(ex2_approx(x0), ex2_approx(x1));
           pk[i] = v;
-          sum += __uint_as_float(v << 16) + __uint_as_float(v & 0xFFFF0000u);
+          sum2 = fadd2(sum2, f2_pack_u(v << 16, v & 0xFFFF0000u));
         }
         tmem_st16(tS + lane_off + c * 16, pk);
       }
+      float s_lo, s_hi;
+      f2_unpack(sum2, s_lo, s_hi);
+      const float sum = s_lo + s_hi;
       l_sum += sum;
       tmem_wait_st();
       tc_fence_before();
