@@ -27,7 +27,7 @@
 
 #include <cudaTypedefs.h>
 
-#include "../../include/upipe.h"
+#include "upipe.h"
 #include "internal.h"
 
 namespace upipe {

@@ -19,7 +19,7 @@
 #include <cmath>
 #include <mutex>
 
-#include "../../include/upipe.h"
+#include "upipe.h"
 #include "internal.h"
 
 namespace upipe {
