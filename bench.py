@@ -352,16 +352,37 @@ def run_ours(a):
 
         e2e_step()
         barrier()
+        # per-phase events (host->device, compute, device->host) of the same steps
+        ph = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(a.steps)]
+
+        def e2e_step_marked(evs):
+            evs[0].record(stream)
+            q.copy_(hq, non_blocking=True)
+            do.copy_(hdo, non_blocking=True)
+            if not kv_host:
+                k_in.copy_(hk, non_blocking=True)
+                v_in.copy_(hv, non_blocking=True)
+            evs[1].record(stream)
+            up.upipe_attn_fwd(q, k_in, v_in, o, lse, B, S, Hq, Hkv, D, 1, hc, T, ws, ws_bytes, stream)
+            up.upipe_attn_bwd(q, k_in, v_in, o, lse, do, dq, dk, dv, B, S, Hq, Hkv, D, 1, hc, T,
+                              ws, ws_bytes, stream)
+            evs[2].record(stream)
+            for hdst, dsrc in zip(outs_h, (o, lse, dq, dk, dv)):
+                hdst.copy_(dsrc, non_blocking=True)
+            evs[3].record(stream)
+
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(a.steps):
-            e2e_step()
+        for i in range(a.steps):
+            e2e_step_marked(ph[i])
         e1.record(stream)
         barrier()
+        breakdown = {k: sum(ev[i].elapsed_time(ev[i + 1]) for ev in ph) / a.steps
+                     for i, k in enumerate(("h2d_ms", "compute_ms", "d2h_ms"))}
         e2e_value, _ = job_throughput(e0.elapsed_time(e1), a.steps, f_fwd + f_bwd, world, red)
         line["e2e"] = {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-                       "d2h_bytes_per_step": int(d2h)}
+                       "d2h_bytes_per_step": int(d2h), "per_step_ms": breakdown}
         up.upipe_sync_status(stream)
 
     if rank == 0 and world == 1 and not a.no_cpu_baseline:

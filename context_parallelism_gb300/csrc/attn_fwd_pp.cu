@@ -156,16 +156,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16(128, 128, false, false);
       const uint32_t id_o = idesc_bf16(128, kD, false, true);
-      const uint32_t sQ = smem_u32(smem + L::kQ);
+      // Descriptors built once; stages and steps are constant offsets (16-byte units).
+      const uint64_t dQ0 = kdesc0(smem_u32(smem + L::kQ));
+      const uint64_t dK0 = kdesc0(smem_u32(smem + L::kK));
+      const uint64_t dV0 = mndesc0(smem_u32(smem + L::kV));
+      constexpr uint32_t kTileU = kTile >> 4;
       bool ok = wait(q_full, 0);
       auto issue_s = [&](int w, int j) -> bool {
         if (w == 0 && !wait(k_full + (j & 1), (j >> 1) & 1)) return false;
         tc_fence_after();
-        const uint32_t sK = smem_u32(smem + L::kK + (j & 1) * kTile);
+        const uint64_t dQ = dQ0 + w * kTileU, dK = dK0 + (j & 1) * kTileU;
+        const uint32_t tS = tmem + 128 * w;
 #pragma unroll
         for (int k16 = 0; k16 < kD / 16; ++k16)
-          umma_f16_ss(tmem + 128 * w, desc_kmajor(sQ + w * kTile, k16), desc_kmajor(sK, k16),
-                      id_s, k16 > 0 ? 1u : 0u);
+          umma_f16_ss(tS, dQ + kstep(k16), dK + kstep(k16), id_s, k16 > 0 ? 1u : 0u);
         umma_commit(s_full + w);
         return true;
       };
@@ -173,12 +177,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait(p_full + w, j & 1)) return false;
         if (w == 0 && !wait(v_full + (j & 1), (j >> 1) & 1)) return false;
         tc_fence_after();
-        const uint32_t sV = smem_u32(smem + L::kV + (j & 1) * kTile);
+        const uint64_t dV = dV0 + (j & 1) * kTileU;
         const uint32_t acc0 = (j > 0 || !a.first) ? 1u : 0u;
         const uint32_t tP = tmem + 128 * w, tO = tmem + 256 + 128 * w;
 #pragma unroll
         for (int k16 = 0; k16 < 8; ++k16)
-          umma_f16_ts(tO, tP + k16 * 8, desc_mnmajor(sV, k16), id_o, k16 > 0 ? 1u : acc0);
+          umma_f16_ts(tO, tP + k16 * 8, dV + mnstep(k16), id_o, k16 > 0 ? 1u : acc0);
         if (j == n_kv - 1) umma_commit(o_done + w);
         return true;
       };

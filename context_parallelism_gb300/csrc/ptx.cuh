@@ -272,6 +272,22 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile_saddr, int k16,
   return sdesc(a, lbo, sbo);
 }
 
+// Issue-path helpers: build a tile's descriptor once, then reach the k-th 16-element step by a
+// constant add to the start-address field (bits 0-13, in 16-byte units). Shared-memory
+// addresses stay below 256 KiB, so the field never carries into its neighbour. This keeps the
+// single MMA-issuing thread at a few instructions per MMA.
+__device__ __forceinline__ uint64_t kdesc0(uint32_t tile_saddr) { return sdesc(tile_saddr, 16u, 1024u); }
+__device__ __forceinline__ uint64_t mndesc0(uint32_t tile_saddr, uint32_t lbo = kBoxBytes,
+                                            uint32_t sbo = 1024u) {
+  return sdesc(tile_saddr, lbo, sbo);
+}
+// K-major step: a new box every 4 steps, 32 bytes within a 128-byte row otherwise.
+__host__ __device__ constexpr uint32_t kstep(int k16, uint32_t box_bytes = kBoxBytes) {
+  return ((static_cast<uint32_t>(k16 >> 2) * box_bytes) + static_cast<uint32_t>(k16 & 3) * 32u) >> 4;
+}
+// MN-major step: 16 reduction rows of 128 bytes.
+__host__ __device__ constexpr uint32_t mnstep(int k16) { return (static_cast<uint32_t>(k16) * 2048u) >> 4; }
+
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 D: D format bits 4-5 = 1,
 // A format bits 7-9 = 1 (bf16), B format bits 10-12 = 1, A MN-major bit 15, B MN-major
 // bit 16, N >> 3 in bits 17-22, M >> 4 in bits 24-28.
