@@ -252,21 +252,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       float mx = -INFINITY;
       if (need_mask) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld32_sync(tS + lane_off + c * 32, r);
+        for (int h = 0; h < 2; ++h) {
+          uint32_t r[64];
+          tmem_ld64_sync(tS + lane_off + h * 64, r);
 #pragma unroll
-          for (int i = 0; i < 32; i += 2)
-            mx = fmax3(mx, (c * 32 + i < lim) ? __uint_as_float(r[i]) : -INFINITY,
-                       (c * 32 + i + 1 < lim) ? __uint_as_float(r[i + 1]) : -INFINITY);
+          for (int i = 0; i < 64; i += 2)
+            mx = fmax3(mx, (h * 64 + i < lim) ? __uint_as_float(r[i]) : -INFINITY,
+                       (h * 64 + i + 1 < lim) ? __uint_as_float(r[i + 1]) : -INFINITY);
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld32_sync(tS + lane_off + c * 32, r);
+        for (int h = 0; h < 2; ++h) {
+          uint32_t r[64];
+          tmem_ld64_sync(tS + lane_off + h * 64, r);
 #pragma unroll
-          for (int i = 0; i < 32; i += 2)
+          for (int i = 0; i < 64; i += 2)
             mx = fmax3(mx, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
         }
       }
@@ -293,30 +293,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float mb = (m_used == -INFINITY) ? 0.f : m_used;
       // Pass 2: P rounded to bf16 once, written over S's first 64 columns; the row sum adds
       // exactly the weights the P.V MMA consumes (paired fp32 adds of the two bf16 halves).
-      // Columns 64..127 are read before any P lands there (P of columns c..c+31 goes to
-      // columns c/2..c/2+15).
+      // Columns 64..127 are read before any P lands there (P of columns c..c+63 goes to
+      // columns c/2..c/2+31).
       const uint64_t sl2 = f2_pack(a.scale_log2, a.scale_log2);
       const uint64_t nm2 = f2_pack(-mb, -mb);
       uint64_t sum2 = f2_pack(0.f, 0.f);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32_sync(tS + lane_off + c * 32, r);
+      for (int h = 0; h < 2; ++h) {
+        uint32_t r[64];
+        tmem_ld64_sync(tS + lane_off + h * 64, r);
         if (need_mask) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (c * 32 + i >= lim) r[i] = __float_as_uint(-INFINITY);
+          for (int i = 0; i < 64; ++i)
+            if (h * 64 + i >= lim) r[i] = __float_as_uint(-INFINITY);
         }
-        uint32_t pk[16];
+        uint32_t pk[32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 32; ++i) {
           float x0, x1;
           f2_unpack(ffma2(f2_pack_u(r[2 * i], r[2 * i + 1]), sl2, nm2), x0, x1);
           const uint32_t v = pack_bf16(ex2_approx(x0), ex2_approx(x1));
           pk[i] = v;
           sum2 = fadd2(sum2, f2_pack_u(v << 16, v & 0xFFFF0000u));
         }
-        tmem_st16(tS + lane_off + c * 16, pk);
+        tmem_st32(tS + lane_off + h * 32, pk);
       }
       float s_lo, s_hi;
       f2_unpack(sum2, s_lo, s_hi);
