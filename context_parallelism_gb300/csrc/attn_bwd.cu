@@ -241,9 +241,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int col = c * 32 + x;
           const int64_t i = q0 + col;
           const bool vis = key_ok && (i < a.S) && (!a.causal || i >= pj);
-          const float pv = vis ? ex2_approx(fmaf(__uint_as_float(rs[x]), a.scale_log2, -lse_s[col])) : 0.f;
+          const float pv = vis ? ex2_approx(fmaf(__uint_as_float(rs[x]), a.scale_log2, lse_s[col])) : 0.f;
           p[x] = pv;
-          ds[x] = pv * fmaf(__uint_as_float(rd[x]), a.scale, -dv_s[col]);
+          ds[x] = pv * fmaf(__uint_as_float(rd[x]), a.scale, dv_s[col]);
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {

@@ -12,6 +12,7 @@
 //   dP^T = V dO^T                tcgen05                         -> TMEM dP
 //   P^T  = exp2(S^T*scale*log2e - LSE*log2e), masked; bf16 back into TMEM S
 //   dS^T = P^T * (scale*dP^T - scale*D)                bf16 -> shared memory (two boxes)
+//   (the pre-pass stores -LSE*log2e and -scale*D, so each is one fused multiply-add)
 //   dV  += P^T dO                tcgen05 with A read from TMEM
 //   dK  += dS^T Q                tcgen05 (A K-major, B MN-major)
 //   dQ^T = K^T dS^T              tcgen05 (M 128 = head dim, N 128)  -> TMEM dP (dP is consumed)
@@ -56,6 +57,18 @@ struct BppLayout {
   static constexpr int kBytes = kAbort + 4;
 };
 static_assert(BppLayout::kBytes <= 232448, "shared memory budget");
+
+// A CTA walks the query tiles q-head outer (of its kv-head's group), tile inner. Each role
+// steps its own cursor through that walk one tile at a time: no division per tile.
+struct Cursor {
+  int head = 0, qt = 0;
+  __device__ void next(int n) {
+    if (++qt == n) {
+      qt = 0;
+      ++head;
+    }
+  }
+};
 
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_pp_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -144,10 +157,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   };
-  auto decode = [&](int it, int& zq, int64_t& q0) {
-    const int hl = kvl * a.G + it / nq;
-    zq = b * a.hc + hl;
-    q0 = static_cast<int64_t>(qt_lo + it % nq) * 128;
+  auto decode = [&](const Cursor& c, int& zq, int64_t& q0) {
+    zq = b * a.hc + kvl * a.G + c.head;
+    q0 = static_cast<int64_t>(qt_lo + c.qt) * 128;
   };
 
   if (warp == 9) {
@@ -164,11 +176,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       int q_issued = 0, d_issued = 0;
       bool ok = true;
-      for (int it = 0; it < n_it; ++it) {
+      Cursor cur;
+      for (int it = 0; it < n_it; ++it, cur.next(nq)) {
         const int st = it & 1;
         int zq;
         int64_t q0;
-        decode(it, zq, q0);
+        decode(cur, zq, q0);
         if (it >= 2 && !wait(qe + st, ((it >> 1) - 1) & 1)) { ok = false; break; }
         mbar_arrive_expect_tx(qf + st, kTile + 1024);
         for (int x = 0; x < 2; ++x)
@@ -290,12 +303,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t sl2 = f2_pack(a.scale_log2, a.scale_log2);
     const uint64_t sc2 = f2_pack(a.scale, a.scale);
     float p[64];  // this group's P^T row of the tile in flight
+    Cursor cur_p, cur_q;  // the tiles do_p and do_dq handle next
     // P^T(i) of this group's columns: S^T -> exp2 -> bf16 back into its own S columns.
     auto do_p = [&](int i) -> bool {
       const int st = i & 1;
       int zq;
       int64_t q0;
-      decode(i, zq, q0);
+      decode(cur_p, zq, q0);
+      cur_p.next(nq);
       const int64_t qc0 = q0 + 64 * w;  // first query row of this group's columns
       const float* lse_s = reinterpret_cast<const float*>(smem + L::kVec + st * 1024) + 64 * w;
       // qf: the LSE/D vectors of this tile landed (the stage is refilled only after dK(i),
@@ -309,10 +324,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld64_sync(tS + lane_off + 64 * w, r);
 #pragma unroll
       for (int x = 0; x < 64; x += 4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(lse_s + x);
+        // -LSE*log2e pairs straight from shared memory as packed fp32x2 operands
+        const ulonglong2 l4 = *reinterpret_cast<const ulonglong2*>(lse_s + x);
         float y0, y1, y2, y3;
-        f2_unpack(ffma2(f2_pack_u(r[x], r[x + 1]), sl2, f2_pack(-l4.x, -l4.y)), y0, y1);
-        f2_unpack(ffma2(f2_pack_u(r[x + 2], r[x + 3]), sl2, f2_pack(-l4.z, -l4.w)), y2, y3);
+        f2_unpack(ffma2(f2_pack_u(r[x], r[x + 1]), sl2, l4.x), y0, y1);
+        f2_unpack(ffma2(f2_pack_u(r[x + 2], r[x + 3]), sl2, l4.y), y2, y3);
         p[x + 0] = ex2_approx(y0);
         p[x + 1] = ex2_approx(y1);
         p[x + 2] = ex2_approx(y2);
@@ -345,15 +361,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld64_sync(tDP + lane_off + 64 * w, r);
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const float4 da = *reinterpret_cast<const float4*>(dv_s + u * 8);
-        const float4 db = *reinterpret_cast<const float4*>(dv_s + u * 8 + 4);
-        const float dvv[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
+        // -scale*D pairs straight from shared memory as packed fp32x2 operands
+        const ulonglong2 da = *reinterpret_cast<const ulonglong2*>(dv_s + u * 8);
+        const ulonglong2 db = *reinterpret_cast<const ulonglong2*>(dv_s + u * 8 + 4);
+        const uint64_t dvv[4] = {da.x, da.y, db.x, db.y};
         uint32_t pk[4];
 #pragma unroll
         for (int x = 0; x < 4; ++x) {
           const int col = u * 8 + 2 * x;
-          const uint64_t t2 = ffma2(f2_pack_u(r[col], r[col + 1]), sc2,
-                                    f2_pack(-dvv[2 * x], -dvv[2 * x + 1]));
+          const uint64_t t2 = ffma2(f2_pack_u(r[col], r[col + 1]), sc2, dvv[x]);
           float d0, d1;
           f2_unpack(fmul2(t2, f2_pack(p[col], p[col + 1])), d0, d1);
           pk[x] = pack_bf16(d0, d1);
@@ -371,7 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto do_dq = [&](int i) -> bool {
       int zq;
       int64_t q0;
-      decode(i, zq, q0);
+      decode(cur_q, zq, q0);
+      cur_q.next(nq);
       const int64_t qc0 = q0 + 64 * w;
       if (!__all_sync(0xffffffffu, wait(dq_full, i & 1))) return false;
       tc_fence_after();
@@ -380,11 +397,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(dq_free);
+      // Query rows past S fall in the accumulator's padding (it has S_pad rows per head, a
+      // multiple of 128) and add exact zeros there (their P is masked to 0): no bound check.
       float* dq_col = a.dqacc + (static_cast<int64_t>(zq) * a.S_pad + qc0) * kD + t;
-      const int64_t n_rows = a.S - qc0;
 #pragma unroll
-      for (int x = 0; x < 64; ++x)
-        if (x < n_rows) red_add_f32(dq_col + x * kD, __uint_as_float(r[x]));
+      for (int x = 0; x < 64; ++x) red_add_f32(dq_col + x * kD, __uint_as_float(r[x]));
       return true;
     };
     // Software-pipelined per group: dS(i), then P(i+1) (overlapping dK(i) and dQ(i) on the

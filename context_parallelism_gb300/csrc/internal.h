@@ -56,8 +56,8 @@ struct BwdArgs {
   int hc, kc, G, Hkv, kvh0;      // group sizes, total kv-heads, first kv-head of the group
   int causal;
   float scale, scale_log2;
-  const float* lse2;             // [B*hc][S_pad] LSE * log2(e)
-  const float* dvec;             // [B*hc][S_pad] scale * D_i,  D_i = <dO_i, O_i>
+  const float* lse2;             // [B*hc][S_pad] -LSE * log2(e)
+  const float* dvec;             // [B*hc][S_pad] -scale * D_i,  D_i = <dO_i, O_i>
   float* dqacc;                  // [B*hc][S_pad][D] fp32 dQ accumulator
   void* dk;                      // [B,S,Hkv,D] bf16
   void* dv;                      // [B,S,Hkv,D] bf16
@@ -85,7 +85,8 @@ cudaError_t launch_head_to_seq(const void* src, void* dst, int B, int64_t S, int
 
 // Backward pre-pass for one head group (q-heads h0 .. h0+hc-1):
 //   dow[b*hc+h][s][:] = dout[b][s][h0+h][:]
-//   dvec[(b*hc+h)*S_pad + s] = scale * sum_d dout*o (fp32), lse2[...] = lse[b][h0+h][s]*log2(e)
+//   dvec[(b*hc+h)*S_pad + s] = -scale * sum_d dout*o (fp32), lse2[...] = -lse[b][h0+h][s]*log2(e)
+//   (stored negated: the kernels add them with one fused multiply-add)
 //   dqacc[(b*hc+h)*S_pad + s][:] = 0
 // rows s in [S, S_pad) get dvec = lse2 = 0 and zeroed dqacc.
 cudaError_t launch_bwd_pre(const void* o, const void* dout, const float* lse, void* dow,

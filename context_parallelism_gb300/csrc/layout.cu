@@ -108,8 +108,8 @@ __global__ void bwd_pre_kernel(const uint4* __restrict__ o, const uint4* __restr
     }
     for (int off = Dc / 2; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
     if (live && c == 0) {
-      dvec[zrow] = (s < S) ? dot * scale : 0.f;
-      lse2[zrow] = (s < S) ? lse[(b * Hq + h0 + h) * S + s] * kLog2e : 0.f;
+      dvec[zrow] = (s < S) ? -(dot * scale) : 0.f;
+      lse2[zrow] = (s < S) ? -(lse[(b * Hq + h0 + h) * S + s] * kLog2e) : 0.f;
     }
   }
 }
