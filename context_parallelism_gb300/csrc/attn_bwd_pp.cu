@@ -20,15 +20,18 @@
 //          warp, added with fire-and-forget fp32 reductions.
 // Compute group w in {0, 1} owns query columns [64w, 64w+64) of every tile. Its packed P^T goes
 // to S columns [64w, 64w+32) (inside the columns it alone reads), and its dS^T to shared box w.
+// A third warpgroup drains dQ^T(i) from TMEM into the fp32 accumulator, off the groups' path.
 //
 // MMA issue order: S(0), dV(0), dP(0), then per tile i: S(i+1), dK(i), dQ(i), dV(i+1), dP(i+1).
-// Each group runs dS(i), P(i+1), dQ(i) read-out in that order, so its dS(i) overlaps S(i+1),
-// its P(i+1) overlaps dK(i) and dQ(i), and its read-out of dQ(i) overlaps dV(i+1). One thread's MMAs execute in order, so S(i+1) overwrites S only after dV(i)
-// has read P^T(i), and the commit that publishes dP(i+1) also covers dK(i) and dQ(i), which read
-// the single dS^T buffer the groups then overwrite.
+// Each group runs dS(i) then P(i+1), so its dS(i) overlaps S(i+1) and its P(i+1) overlaps dK(i)
+// and dQ(i); the drain reads dQ(i) while dV(i+1) runs. One thread's MMAs execute in order, so
+// S(i+1) overwrites S only after dV(i) has read P^T(i), and the commit that publishes dP(i+1)
+// also covers dK(i) and dQ(i), which read the single dS^T buffer the groups then overwrite.
 //
-// Threads (320): warps 0-3 compute group 0, warps 4-7 compute group 1, warp 8 TMEM + MMA issue,
-// warp 9 TMA producer. TMEM: dV [0,128), dK [128,256), S [256,384), dP/dQ [384,512).
+// Threads (512): warps 0-3 compute group 0, warps 4-7 compute group 1, warps 8-11 dQ drain,
+// warp 12 TMEM + MMA issue, warp 13 TMA producer, warps 14-15 idle. Registers move from the
+// drain to the compute groups (152 / 152 / 80 / 128 per thread).
+// TMEM: dV [0,128), dK [128,256), S [256,384), dP/dQ [384,512).
 // Shared memory (231.6 KB, no alignment slack: the dynamic window must start 1 KiB-aligned,
 // which is checked): K, V, two Q and two dO stages, dS^T, two LSE/D vector stages, barriers.
 #include <cfloat>
@@ -40,7 +43,7 @@ namespace upipe {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kThreads = 320;
+constexpr int kThreads = 512;
 constexpr int kTile = 128 * kD * 2;  // 32 KiB
 
 struct BppLayout {
@@ -93,7 +96,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* dq_full = bar + 11;
   uint64_t* p_ready = bar + 12;  // 8 warp arrivals
   uint64_t* ds_ready = bar + 13; // 8
-  uint64_t* dq_free = bar + 14;  // 8
+  uint64_t* dq_free = bar + 14;  // 4 drain-warp arrivals
   uint64_t* done = bar + 15;
   uint64_t* drain = bar + 16;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kSlot);
@@ -125,13 +128,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(dq_full, 1);
     mbar_init(p_ready, 8);
     mbar_init(ds_ready, 8);
-    mbar_init(dq_free, 8);
+    mbar_init(dq_free, 4);
     mbar_init(done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 8) {
+  if (warp == 12) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -162,7 +165,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     q0 = static_cast<int64_t>(qt_lo + c.qt) * 128;
   };
 
-  if (warp == 9) {
+  // Launched with 512 x 128 registers. The MMA/TMA warpgroup keeps 128, the dQ drain gives up
+  // 48 and each compute group takes 24 more: 128 * (128 + 80 + 2 * 152) = 65536, exactly the
+  // launch's pool. Each role's code sits inside the branch that sets its count, so the compiler
+  // allocates that code for it.
+  if (warp >= 12) {
+  if (warp == 13) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -207,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait(df + (it & 1), (it >> 1) & 1, 100000000ull);
       }
     }
-  } else if (warp == 8) {
+  } else if (warp == 12) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       const uint32_t id_kk = idesc_bf16(128, 128, false, false);  // S^T, dP^T
@@ -292,10 +300,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(drain, 0, 100000000ull);
       }
     }
+  }  // warps 14-15: idle, they only complete the warpgroup of the MMA and TMA warps
+  } else if (warp >= 8) {
+    setmaxnreg_dec<80>();
+    // ---------------- dQ drain ----------------
+    // dQ^T(i): lane t = head-dim index d, column c = query row q0 + c. Each warp adds one
+    // contiguous 128-byte line per query row, fire-and-forget: the first 64 columns, then the
+    // last 64, after which the columns are released (dP(i+1) reuses them; it is issued behind
+    // dV(i+1), which covers the first half's reductions). Query rows past S fall in the
+    // accumulator's padding (S_pad rows per head, a multiple of 128) and add exact zeros there
+    // (their P is masked to 0), so no bound check.
+    const int t = threadIdx.x & 127;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    Cursor cur;
+    for (int i = 0; i < n_it; ++i, cur.next(nq)) {
+      if (!__all_sync(0xffffffffu, wait(dq_full, i & 1))) break;
+      tc_fence_after();
+      int zq;
+      int64_t q0;
+      decode(cur, zq, q0);
+      float* dq_col = a.dqacc + (static_cast<int64_t>(zq) * a.S_pad + q0) * kD + t;
+      uint32_t r[64];
+      tmem_ld64_sync(tDP + lane_off, r);
+#pragma unroll
+      for (int x = 0; x < 64; ++x) red_add_f32(dq_col + x * kD, __uint_as_float(r[x]));
+      tmem_ld64_sync(tDP + lane_off + 64, r);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dq_free);
+#pragma unroll
+      for (int x = 0; x < 64; ++x) red_add_f32(dq_col + (64 + x) * kD, __uint_as_float(r[x]));
+    }
   } else {
+    setmaxnreg_inc<152>();
     // ---------------- compute groups ----------------
     const int w = warp >> 2;              // owns query columns [64w, 64w+64)
-    const int t = threadIdx.x & 127;      // key row (S^T/dP^T lanes) / head dim (dQ^T lanes)
+    const int t = threadIdx.x & 127;      // key row (S^T/dP^T lanes)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t sDS = smem_u32(smem + L::kDS + w * kBoxBytes);
     const int64_t pj = p0 + t;
@@ -303,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t sl2 = f2_pack(a.scale_log2, a.scale_log2);
     const uint64_t sc2 = f2_pack(a.scale, a.scale);
     float p[64];  // this group's P^T row of the tile in flight
-    Cursor cur_p, cur_q;  // the tiles do_p and do_dq handle next
+    Cursor cur_p;  // the tile do_p handles next
     // P^T(i) of this group's columns: S^T -> exp2 -> bf16 back into its own S columns.
     auto do_p = [&](int i) -> bool {
       const int st = i & 1;
@@ -382,36 +422,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(ds_ready);
       return true;
     };
-    // dQ^T(i): lane t = head-dim index d, column c = query row qc0 + c. The TMEM columns are
-    // released as soon as they are in registers; the reductions drain behind the next MMAs.
-    auto do_dq = [&](int i) -> bool {
-      int zq;
-      int64_t q0;
-      decode(cur_q, zq, q0);
-      cur_q.next(nq);
-      const int64_t qc0 = q0 + 64 * w;
-      if (!__all_sync(0xffffffffu, wait(dq_full, i & 1))) return false;
-      tc_fence_after();
-      uint32_t r[64];
-      tmem_ld64_sync(tDP + lane_off + 64 * w, r);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(dq_free);
-      // Query rows past S fall in the accumulator's padding (it has S_pad rows per head, a
-      // multiple of 128) and add exact zeros there (their P is masked to 0): no bound check.
-      float* dq_col = a.dqacc + (static_cast<int64_t>(zq) * a.S_pad + qc0) * kD + t;
-#pragma unroll
-      for (int x = 0; x < 64; ++x) red_add_f32(dq_col + x * kD, __uint_as_float(r[x]));
-      return true;
-    };
-    // Software-pipelined per group: dS(i), then P(i+1) (overlapping dK(i) and dQ(i) on the
-    // tensor pipe), then the read-out of dQ(i) (overlapping dV(i+1)). P(i+1) overwrites p[]
-    // only after dS(i) has consumed it.
+    // Software-pipelined per group: dS(i), then P(i+1), which overlaps dK(i) and dQ(i) on the
+    // tensor pipe. P(i+1) overwrites p[] only after dS(i) has consumed it.
     bool good = n_it == 0 || do_p(0);
     for (int i = 0; good && i < n_it; ++i) {
       good = do_ds(i);
       if (good && i + 1 < n_it) good = do_p(i + 1);
-      if (good) good = do_dq(i);
     }
     if (good && n_it > 0) {
       good = __all_sync(0xffffffffu, wait(done, 0));
@@ -447,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == 12) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
