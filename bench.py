@@ -51,6 +51,42 @@ def _args():
     return ap.parse_args()
 
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch, from a one-pass ncu
+# capture of the first launch of each attention kernel on the default workload (one launch =
+# one head group over the whole sequence). A figure holds only for the kernel source file it was
+# taken on (by SHA-256) and for that workload; otherwise the bench reports null.
+TRAFFIC = {
+    "attn_bwd": {"workload": "llama8b_s128k", "head_chunk": 8, "seq_trunk": 131072,
+                 "files": ["context_parallelism_gb300/csrc/attn_bwd_pp.cu"],
+                 "sha256": "acb986ccab2e2549748f59176ffe93b8481839fdc12dd3d0b1903e135058d2d1",
+                 "bytes": 4414092800 + 2199979520},
+    "attn_fwd": {"workload": "llama8b_s128k", "head_chunk": 8, "seq_trunk": 131072,
+                 "files": ["context_parallelism_gb300/csrc/attn_fwd_pp.cu"],
+                 "sha256": "0713983e754a3824059786d3d907b86a92439aa782f81362962e520b6c399c1b",
+                 "bytes": 928111872 + 255031552},
+}
+
+
+def source_hash(files):
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def traffic_per_launch(kernel, workload, head_chunk, seq_trunk):
+    """The captured DRAM bytes per launch of `kernel`, or None when the capture does not
+    apply (other workload or schedule, kernel source changed since, or no capture)."""
+    t = TRAFFIC.get(kernel)
+    if not t or t["bytes"] is None:
+        return None
+    if (t["workload"], t["head_chunk"], t["seq_trunk"]) != (workload, head_chunk, seq_trunk):
+        return None
+    return t["bytes"] if source_hash(t["files"]) == t["sha256"] else None
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -299,7 +335,8 @@ def run_ours(a):
                     "unit": "TFLOP/s", "frac": achieved / peak,
                     "peak_source": f"{peak_src} bf16_tflops_sustained",
                     "launches": n_launch, "avg_launch_ms": tot_ms / max(n_launch, 1),
-                    "traffic": None}
+                    "traffic": traffic_per_launch(top, w.name, hc, T),
+                    "traffic_unit": "bytes per launch"}
     else:
         roofline = {"kernel": top, "bound": "hbm", "achieved": None, "peak": peaks["hbm_gbs"],
                     "unit": "GB/s", "frac": None, "traffic": None}
