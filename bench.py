@@ -48,6 +48,12 @@ def _args():
                     help="print one JSON line per sweep point instead of the bench line: "
                          "chunk-trunk = head_chunk x seq_trunk grid; host-kv = the same "
                          "workload with K/V on the device and in pinned host memory")
+    ap.add_argument("--head-chunks", default=None,
+                    help="comma-separated head_chunk values for --sweep (default: per sweep)")
+    ap.add_argument("--seq-trunks", default=None,
+                    help="comma-separated seq_trunk values for --sweep (default: per sweep)")
+    ap.add_argument("--kv-modes", default=None,
+                    help="for --sweep host-kv: comma-separated subset of device,host")
     return ap.parse_args()
 
 
@@ -445,13 +451,20 @@ def run_sweep(a):
         w = w.with_(S=a.seq_len, seq_trunk=min(w.seq_trunk, a.seq_len))
     dev = torch.device("cuda", 0)
     q, k, v, do = (t.to(dev) for t in make_inputs(w, "cuda" if w.gen_device == "cuda" else "cpu"))
+    def ints(text, default):
+        return [int(x) for x in text.split(",")] if text else list(default)
+
     if a.sweep == "chunk-trunk":
-        grid = sorted({(hc, T) for hc in (4, 8, 16, 32) if hc % w.G == 0 and w.Hq % hc == 0
-                       for T in (16384, 32768, w.S) if T <= w.S})
+        hcs = ints(a.head_chunks, (4, 8, 16, 32))
+        Ts = ints(a.seq_trunks, (16384, 32768, w.S))
+        grid = sorted({(hc, T) for hc in hcs if hc % w.G == 0 and w.Hq % hc == 0
+                       for T in Ts if T <= w.S})
         kv_modes = [False]
     else:
-        grid = [(a.head_chunk or w.head_chunk, a.seq_trunk or w.seq_trunk)]
-        kv_modes = [False, True]
+        grid = [(hc, T) for hc in ints(a.head_chunks, [a.head_chunk or w.head_chunk])
+                for T in ints(a.seq_trunks, [a.seq_trunk or w.seq_trunk])]
+        modes = (a.kv_modes or "device,host").split(",")
+        kv_modes = [m == "host" for m in modes]
     for kv_host in kv_modes:
         if kv_host:
             kk = torch.empty(k.shape, dtype=k.dtype, pin_memory=True)
@@ -477,10 +490,13 @@ def run_sweep(a):
             def bwd():
                 up.upipe_attn_bwd(q, kk, vv, o, lse, do, dq, dk, dv, *args, ws, ws_b)
 
+            torch.cuda.synchronize()
+            free0 = torch.cuda.mem_get_info()[0]
             for _ in range(max(1, a.warmup)):
                 fwd()
                 bwd()
             torch.cuda.synchronize()
+            lib_alloc = free0 - torch.cuda.mem_get_info()[0]
             e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
             tf = tb = 0.0
             for _ in range(a.steps):
@@ -498,7 +514,10 @@ def run_sweep(a):
                 "sweep": a.sweep, "workload": w.name, "S": w.S, "head_chunk": hc,
                 "seq_trunk": T, "kv_on_host": kv_host, "fwd_tflops": ff / tf / 1e9,
                 "bwd_tflops": fb / tb / 1e9, "fwdbwd_tflops": (ff + fb) / (tf + tb) / 1e9,
-                "ms_per_step": (tf + tb) / a.steps, "workspace_gb": ws_b / 1e9}), flush=True)
+                "ms_per_step": (tf + tb) / a.steps, "workspace_gb": ws_b / 1e9,
+                "workspace_unchunked_gb": up.upipe_workspace_bytes(
+                    w.B, w.S, w.Hq, w.Hkv, w.D, 1, w.Hq, T, up.UPIPE_PASS_BOTH, kv_host) / 1e9,
+                "device_bytes_allocated_by_calls": int(lib_alloc)}), flush=True)
             del ws
 
 

@@ -22,9 +22,9 @@
 // to S columns [64w, 64w+32) (inside the columns it alone reads), and its dS^T to shared box w.
 // A third warpgroup drains dQ^T(i) from TMEM into the fp32 accumulator, off the groups' path.
 //
-// MMA issue order: S(0), dV(0), dP(0), then per tile i: S(i+1), dK(i), dQ(i), dV(i+1), dP(i+1).
-// Each group runs dS(i) then P(i+1), so its dS(i) overlaps S(i+1) and its P(i+1) overlaps dK(i)
-// and dQ(i); the drain reads dQ(i) while dV(i+1) runs. One thread's MMAs execute in order, so
+// MMA issue order: S(0), dV(0), dP(0), then per tile i: S(i+1), dQ(i), dK(i), dV(i+1), dP(i+1).
+// Each group runs dS(i) then P(i+1), so its dS(i) overlaps S(i+1) and its P(i+1) overlaps dQ(i)
+// and dK(i); the drain reads dQ(i) while dK(i) and dV(i+1) run (dQ goes first for that). One thread's MMAs execute in order, so
 // S(i+1) overwrites S only after dV(i) has read P^T(i), and the commit that publishes dP(i+1)
 // also covers dK(i) and dQ(i), which read the single dS^T buffer the groups then overwrite.
 //
@@ -278,12 +278,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t acc0 = i > 0 ? 1u : 0u;
 #pragma unroll
         for (int k16 = 0; k16 < 8; ++k16)
-          umma_f16_ss(tDK, dDSk + kstep(k16), dQ + mnstep(k16), id_kmn, k16 > 0 ? 1u : acc0);
-        umma_commit(qe + st);
-#pragma unroll
-        for (int k16 = 0; k16 < 8; ++k16)
           umma_f16_ss(tDP, dKmn + mnstep(k16), dDSmn + mnstep(k16), id_mnmn, k16 > 0 ? 1u : 0u);
         umma_commit(dq_full);
+#pragma unroll
+        for (int k16 = 0; k16 < 8; ++k16)
+          umma_f16_ss(tDK, dDSk + kstep(k16), dQ + mnstep(k16), id_kmn, k16 > 0 ? 1u : acc0);
+        umma_commit(qe + st);
         return true;
       };
 

@@ -249,7 +249,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Pass 1 over S (TMEM): the row maximum. Keeping the row in TMEM and reading it twice
       // keeps the softmax within the 168 registers a 10-warp CTA allows. Only tiles that
       // straddle the diagonal or an end pay for the mask.
-      float mx = -INFINITY;
+      // Four independent running maxima keep the dependent chain short (16 steps per half).
+      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (need_mask) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -257,8 +258,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld64_sync(tS + lane_off + h * 64, r);
 #pragma unroll
           for (int i = 0; i < 64; i += 2)
-            mx = fmax3(mx, (h * 64 + i < lim) ? __uint_as_float(r[i]) : -INFINITY,
-                       (h * 64 + i + 1 < lim) ? __uint_as_float(r[i + 1]) : -INFINITY);
+            mq[(i >> 1) & 3] =
+                fmax3(mq[(i >> 1) & 3], (h * 64 + i < lim) ? __uint_as_float(r[i]) : -INFINITY,
+                      (h * 64 + i + 1 < lim) ? __uint_as_float(r[i + 1]) : -INFINITY);
         }
       } else {
 #pragma unroll
@@ -267,9 +269,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld64_sync(tS + lane_off + h * 64, r);
 #pragma unroll
           for (int i = 0; i < 64; i += 2)
-            mx = fmax3(mx, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+            mq[(i >> 1) & 3] =
+                fmax3(mq[(i >> 1) & 3], __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
         }
       }
+      const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
       const float m_new = fmaxf(m_used, mx * a.scale_log2);
       float alpha = 1.f;
       const bool upd = m_new > m_used + kRescaleLog2;
@@ -297,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // columns c/2..c/2+31).
       const uint64_t sl2 = f2_pack(a.scale_log2, a.scale_log2);
       const uint64_t nm2 = f2_pack(-mb, -mb);
-      uint64_t sum2 = f2_pack(0.f, 0.f);
+      uint64_t sum2 = f2_pack(0.f, 0.f), sum2b = f2_pack(0.f, 0.f);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t r[64];
@@ -314,12 +318,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           f2_unpack(ffma2(f2_pack_u(r[2 * i], r[2 * i + 1]), sl2, nm2), x0, x1);
           const uint32_t v = pack_bf16(ex2_approx(x0), ex2_approx(x1));
           pk[i] = v;
-          sum2 = fadd2(sum2, f2_pack_u(v << 16, v & 0xFFFF0000u));
+          // two independent sums halve the dependent add chain
+          if (i & 1)
+            sum2b = fadd2(sum2b, f2_pack_u(v << 16, v & 0xFFFF0000u));
+          else
+            sum2 = fadd2(sum2, f2_pack_u(v << 16, v & 0xFFFF0000u));
         }
         tmem_st32(tS + lane_off + h * 32, pk);
       }
       float s_lo, s_hi;
-      f2_unpack(sum2, s_lo, s_hi);
+      f2_unpack(fadd2(sum2, sum2b), s_lo, s_hi);
       const float sum = s_lo + s_hi;
       l_sum += sum;
       tmem_wait_st();
