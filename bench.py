@@ -53,7 +53,8 @@ def _args():
     ap.add_argument("--seq-trunks", default=None,
                     help="comma-separated seq_trunk values for --sweep (default: per sweep)")
     ap.add_argument("--kv-modes", default=None,
-                    help="for --sweep host-kv: comma-separated subset of device,host")
+                    help="for --sweep host-kv: comma-separated subset of device,host,host+dkdv "
+                         "(host+dkdv: dK/dV in pinned host memory as well)")
     return ap.parse_args()
 
 
@@ -64,12 +65,12 @@ def _args():
 TRAFFIC = {
     "attn_bwd": {"workload": "llama8b_s128k", "head_chunk": 8, "seq_trunk": 131072,
                  "files": ["context_parallelism_gb300/csrc/attn_bwd_pp.cu"],
-                 "sha256": "acb986ccab2e2549748f59176ffe93b8481839fdc12dd3d0b1903e135058d2d1",
-                 "bytes": 4414092800 + 2199979520},
+                 "sha256": "13297857ea532137503734579e763afd5925a5f22e24e4aa498b38d42ada3cc5",
+                 "bytes": 4340129280 + 2160602880},
     "attn_fwd": {"workload": "llama8b_s128k", "head_chunk": 8, "seq_trunk": 131072,
                  "files": ["context_parallelism_gb300/csrc/attn_fwd_pp.cu"],
-                 "sha256": "0713983e754a3824059786d3d907b86a92439aa782f81362962e520b6c399c1b",
-                 "bytes": 928111872 + 255031552},
+                 "sha256": "16c044125171ac7d11a60e4011427ddfd417144aab83888fe40383459cb4c49d",
+                 "bytes": 917466624 + 255216896},
 }
 
 
@@ -459,13 +460,14 @@ def run_sweep(a):
         Ts = ints(a.seq_trunks, (16384, 32768, w.S))
         grid = sorted({(hc, T) for hc in hcs if hc % w.G == 0 and w.Hq % hc == 0
                        for T in Ts if T <= w.S})
-        kv_modes = [False]
+        kv_modes = ["device"]
     else:
         grid = [(hc, T) for hc in ints(a.head_chunks, [a.head_chunk or w.head_chunk])
                 for T in ints(a.seq_trunks, [a.seq_trunk or w.seq_trunk])]
-        modes = (a.kv_modes or "device,host").split(",")
-        kv_modes = [m == "host" for m in modes]
-    for kv_host in kv_modes:
+        kv_modes = (a.kv_modes or "device,host").split(",")
+    for mode in kv_modes:
+        kv_host = mode in ("host", "host+dkdv")
+        dkdv_host = mode == "host+dkdv"
         if kv_host:
             kk = torch.empty(k.shape, dtype=k.dtype, pin_memory=True)
             kk.copy_(k)
@@ -480,8 +482,12 @@ def run_sweep(a):
             o = torch.empty_like(q)
             lse = torch.empty((w.B, w.Hq, w.S), dtype=torch.float32, device=dev)
             dq = torch.empty_like(q)
-            dk = torch.empty_like(k)
-            dv = torch.empty_like(v)
+            if dkdv_host:
+                dk = torch.empty(k.shape, dtype=k.dtype, pin_memory=True)
+                dv = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+            else:
+                dk = torch.empty_like(k)
+                dv = torch.empty_like(v)
             args = (w.B, w.S, w.Hq, w.Hkv, w.D, 1, hc, T)
 
             def fwd():
@@ -512,7 +518,8 @@ def run_sweep(a):
             ff, fb = w.flops_fwd() * a.steps, w.flops_bwd() * a.steps
             print(json.dumps({
                 "sweep": a.sweep, "workload": w.name, "S": w.S, "head_chunk": hc,
-                "seq_trunk": T, "kv_on_host": kv_host, "fwd_tflops": ff / tf / 1e9,
+                "seq_trunk": T, "kv_on_host": kv_host, "dkdv_on_host": dkdv_host,
+                "fwd_tflops": ff / tf / 1e9,
                 "bwd_tflops": fb / tb / 1e9, "fwdbwd_tflops": (ff + fb) / (tf + tb) / 1e9,
                 "ms_per_step": (tf + tb) / a.steps, "workspace_gb": ws_b / 1e9,
                 "workspace_unchunked_gb": up.upipe_workspace_bytes(

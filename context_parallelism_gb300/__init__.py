@@ -229,16 +229,21 @@ def attention_forward(q, k, v, causal=True, head_chunk=None, seq_trunk=None, wor
 
 
 def attention_backward(q, k, v, o, lse, dout, causal=True, head_chunk=None, seq_trunk=None,
-                       workspace=None, stream=None):
-    """dq, dk, dv for the forward above (dk/dv are device tensors even for host k/v)."""
+                       workspace=None, stream=None, dkdv_on_host=False):
+    """dq, dk, dv for the forward above. dk/dv are device tensors, or pinned host tensors when
+    dkdv_on_host (which needs host k/v): then each trunk's dK/dV is copied out as it finishes."""
     import torch
     B, S, Hq, Hkv, D = _dims(q, k)
     hc = head_chunk or Hq
     T = seq_trunk or S
     kv_host = not k.is_cuda
     dq = torch.empty_like(q)
-    dk = torch.empty((B, S, Hkv, D), dtype=q.dtype, device=q.device)
-    dv = torch.empty((B, S, Hkv, D), dtype=q.dtype, device=q.device)
+    if dkdv_on_host:
+        dk = torch.empty((B, S, Hkv, D), dtype=q.dtype, pin_memory=True)
+        dv = torch.empty((B, S, Hkv, D), dtype=q.dtype, pin_memory=True)
+    else:
+        dk = torch.empty((B, S, Hkv, D), dtype=q.dtype, device=q.device)
+        dv = torch.empty((B, S, Hkv, D), dtype=q.dtype, device=q.device)
     need = upipe_workspace_bytes(B, S, Hq, Hkv, D, causal, hc, T, UPIPE_PASS_BWD, kv_host)
     if need == 0:
         upipe_attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, S, Hq, Hkv, D, causal, hc, T, 0, 0,

@@ -61,7 +61,10 @@ struct DevState {
   cudaStream_t copy = nullptr;
   cudaEvent_t slot_ready[2] = {nullptr, nullptr};
   cudaEvent_t slot_free[2] = {nullptr, nullptr};
+  cudaEvent_t dkdv_done[2] = {nullptr, nullptr};  // a dK/dV slot is written (compute stream)
+  cudaEvent_t dkdv_free[2] = {nullptr, nullptr};  // its copy to the host is done (copy stream)
   cudaEvent_t entry = nullptr;
+  cudaEvent_t copy_done = nullptr;
   uint32_t* err = nullptr;  // 256-byte status word allocation
 };
 constexpr int kMaxDev = 64;
@@ -76,8 +79,11 @@ int dev_state(int dev, DevState** out) {
     for (int i = 0; i < 2; ++i) {
       UPIPE_CUDA(cudaEventCreateWithFlags(&d.slot_ready[i], cudaEventDisableTiming));
       UPIPE_CUDA(cudaEventCreateWithFlags(&d.slot_free[i], cudaEventDisableTiming));
+      UPIPE_CUDA(cudaEventCreateWithFlags(&d.dkdv_done[i], cudaEventDisableTiming));
+      UPIPE_CUDA(cudaEventCreateWithFlags(&d.dkdv_free[i], cudaEventDisableTiming));
     }
     UPIPE_CUDA(cudaEventCreateWithFlags(&d.entry, cudaEventDisableTiming));
+    UPIPE_CUDA(cudaEventCreateWithFlags(&d.copy_done, cudaEventDisableTiming));
     UPIPE_CUDA(cudaMalloc(&d.err, 256));
     UPIPE_CUDA(cudaMemset(d.err, 0, 256));
     UPIPE_CUDA(cudaDeviceSynchronize());
@@ -179,6 +185,7 @@ struct Plan {
   size_t f_state_o = 0, f_state_ml = 0, f_total = 0;
   // backward segments
   size_t b_qw = 0, b_dow = 0, b_kw = 0, b_vw = 0, b_slot_k[2] = {0, 0}, b_slot_v[2] = {0, 0};
+  size_t b_slot_dk[2] = {0, 0}, b_slot_dv[2] = {0, 0};  // host-K/V mode: dK/dV trunk slots
   size_t b_dqacc = 0, b_lse2 = 0, b_dvec = 0, b_total = 0;
 };
 
@@ -238,6 +245,8 @@ int make_plan(int B, int64_t S, int Hq, int Hkv, int D, int causal, int head_chu
   p->b_dow = take(qw);
   if (p->kv_host) {
     for (int i = 0; i < 2; ++i) { p->b_slot_k[i] = take(slot); p->b_slot_v[i] = take(slot); }
+    // dK/dV of a trunk land here when dk/dv are pinned host memory too
+    for (int i = 0; i < 2; ++i) { p->b_slot_dk[i] = take(slot); p->b_slot_dv[i] = take(slot); }
   } else {
     p->b_kw = take(kvw);
     p->b_vw = take(kvw);
@@ -303,6 +312,20 @@ int stage_trunk(const Plan& p, const void* src, uint8_t* slot, int kvh0, int64_t
       UPIPE_CUDA(cudaMemcpy2DAsync(d, row, s, static_cast<size_t>(p.Hkv) * row, row,
                                    static_cast<size_t>(Tn), cudaMemcpyHostToDevice, copy));
     }
+  return UPIPE_OK;
+}
+
+// Device -> host copy of one trunk's dK or dV, slot [B][Tn][kc][D] -> token-major rows
+// [t0, t0+Tn) of kv-heads kvh0..kvh0+kc of dst [B,S,Hkv,D]: one 2-D copy per batch row.
+int unstage_trunk(const Plan& p, const uint8_t* slot, void* dst, int kvh0, int64_t t0, int64_t Tn,
+                  cudaStream_t copy) {
+  const size_t row = static_cast<size_t>(p.D) * 2, w = row * p.kc;
+  for (int b = 0; b < p.B; ++b) {
+    uint8_t* d = static_cast<uint8_t*>(dst) + ((static_cast<size_t>(b) * p.S + t0) * p.Hkv + kvh0) * row;
+    const uint8_t* s = slot + static_cast<size_t>(b) * Tn * w;
+    UPIPE_CUDA(cudaMemcpy2DAsync(d, static_cast<size_t>(p.Hkv) * row, s, w, w,
+                                 static_cast<size_t>(Tn), cudaMemcpyDeviceToHost, copy));
+  }
   return UPIPE_OK;
 }
 
@@ -479,12 +502,22 @@ int upipe_attn_bwd(const void* q, const void* k, const void* v, const void* o, c
   Plan p0;
   int st = make_plan(B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk, 0, &p0);
   if (st != UPIPE_OK) return st;
-  const void* dptrs[8] = {q, o, lse, dout, dq, dk, dv, workspace};
-  const char* names[8] = {"q", "o", "lse", "dout", "dq", "dk", "dv", "workspace"};
+  const void* dptrs[6] = {q, o, lse, dout, dq, workspace};
+  const char* names[6] = {"q", "o", "lse", "dout", "dq", "workspace"};
   bool kv_host = false;
   int dev = 0;
-  st = check_placement(dptrs, 8, names, k, v, &kv_host, &dev);
+  st = check_placement(dptrs, 6, names, k, v, &kv_host, &dev);
   if (st != UPIPE_OK) return st;
+  // dk/dv: device memory, or (with host k/v) both pinned host memory, written trunk by trunk
+  int ddk = -1, ddv = -1;
+  const int kdk = pointer_kind(dk, &ddk), kdv = pointer_kind(dv, &ddv);
+  if (kdk != kdv || kdk < 0)
+    return fail(UPIPE_ERR_INVALID_ARG, "dk and dv must both be device memory or both pinned host memory");
+  if (kdk == 0 && (ddk != dev || ddv != dev))
+    return fail(UPIPE_ERR_INVALID_ARG, "dk/dv are on another device");
+  const bool dkdv_host = kdk == 1;
+  if (dkdv_host && !kv_host)
+    return fail(UPIPE_ERR_INVALID_ARG, "dk/dv may be pinned host memory only when k/v are too");
   Plan p;
   make_plan(B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk, kv_host ? 1 : 0, &p);
   if (workspace_bytes < p.b_total)
@@ -537,11 +570,20 @@ int upipe_attn_bwd(const void* q, const void* k, const void* v, const void* o, c
       a.S = S; a.S_pad = p.S_pad;
       a.hc = p.hc; a.kc = p.kc; a.G = p.G; a.Hkv = Hkv; a.kvh0 = kvh0;
       a.causal = causal; a.scale = scale; a.scale_log2 = scale * 1.4426950408889634f;
-      a.lse2 = lse2; a.dvec = dvec; a.dqacc = dqacc; a.dk = dk; a.dv = dv; a.err = ds->err;
+      a.lse2 = lse2; a.dvec = dvec; a.dqacc = dqacc; a.err = ds->err;
+      const int s = job & 1;
+      if (dkdv_host) {
+        // the slot's previous trunk must have reached the host before it is overwritten
+        if (job >= 2) UPIPE_CUDA(cudaStreamWaitEvent(stream, ds->dkdv_free[s], 0));
+        a.dk = ws + p.b_slot_dk[s]; a.dv = ws + p.b_slot_dv[s];
+        a.dkv_rows = Tn; a.dkv_row0 = t0; a.dkv_heads = p.kc; a.dkv_head0 = 0;
+      } else {
+        a.dk = dk; a.dv = dv;
+        a.dkv_rows = S; a.dkv_row0 = 0; a.dkv_heads = Hkv; a.dkv_head0 = kvh0;
+      }
       if (kv_host) {
         st = stg.before(job);
         if (st != UPIPE_OK) return st;
-        const int s = job & 1;
         UPIPE_CUDA(make_tmap_bf16(&tk, stg.slot_k[s], D, Tn, static_cast<int64_t>(B) * p.kc));
         UPIPE_CUDA(make_tmap_bf16(&tv, stg.slot_v[s], D, Tn, static_cast<int64_t>(B) * p.kc));
         a.kv_row_lo = 0; a.kv_row_hi = Tn; a.kv_pos0 = t0;
@@ -553,8 +595,23 @@ int upipe_attn_bwd(const void* q, const void* k, const void* v, const void* o, c
         st = stg.after(job);
         if (st != UPIPE_OK) return st;
       }
+      if (dkdv_host) {
+        // this trunk's dK/dV are final: copy them out on the copy stream
+        UPIPE_CUDA(cudaEventRecord(ds->dkdv_done[s], stream));
+        UPIPE_CUDA(cudaStreamWaitEvent(ds->copy, ds->dkdv_done[s], 0));
+        st = unstage_trunk(p, ws + p.b_slot_dk[s], dk, kvh0, t0, Tn, ds->copy);
+        if (st != UPIPE_OK) return st;
+        st = unstage_trunk(p, ws + p.b_slot_dv[s], dv, kvh0, t0, Tn, ds->copy);
+        if (st != UPIPE_OK) return st;
+        UPIPE_CUDA(cudaEventRecord(ds->dkdv_free[s], ds->copy));
+      }
     }
     UPIPE_CUDA(launch_dq_convert(dqacc, dq, B, S, p.S_pad, Hq, D, h0, p.hc, stream));
+  }
+  if (dkdv_host) {
+    // the caller's stream completes only after the last dK/dV trunk reached the host
+    UPIPE_CUDA(cudaEventRecord(ds->copy_done, ds->copy));
+    UPIPE_CUDA(cudaStreamWaitEvent(stream, ds->copy_done, 0));
   }
   return UPIPE_OK;
 }
@@ -638,8 +695,11 @@ void upipe_shutdown(void) {
     for (int s = 0; s < 2; ++s) {
       cudaEventDestroy(d.slot_ready[s]);
       cudaEventDestroy(d.slot_free[s]);
+      cudaEventDestroy(d.dkdv_done[s]);
+      cudaEventDestroy(d.dkdv_free[s]);
     }
     cudaEventDestroy(d.entry);
+    cudaEventDestroy(d.copy_done);
     cudaFree(d.err);
     d = DevState{};
   }

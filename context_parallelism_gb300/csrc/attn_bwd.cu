@@ -286,7 +286,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (good) tc_fence_after();
     }
     if (good) {
-      const int64_t off = ((static_cast<int64_t>(b) * a.S + pj) * a.Hkv + a.kvh0 + kvl) * D;
+      const int64_t off =
+          ((static_cast<int64_t>(b) * a.dkv_rows + pj - a.dkv_row0) * a.dkv_heads + a.dkv_head0 +
+           kvl) * D;
       __nv_bfloat16* dvrow = static_cast<__nv_bfloat16*>(a.dv) + off;
       __nv_bfloat16* dkrow = static_cast<__nv_bfloat16*>(a.dk) + off;
       const bool store = key_ok && pj < a.S;

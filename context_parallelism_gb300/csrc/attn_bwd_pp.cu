@@ -437,7 +437,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // group 0 writes dV, group 1 writes dK (both already carry their final scaling)
       const uint32_t tAcc = w == 0 ? tDV : tDK;
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(w == 0 ? a.dv : a.dk) +
-                           ((static_cast<int64_t>(b) * a.S + pj) * a.Hkv + a.kvh0 + kvl) * kD;
+                           ((static_cast<int64_t>(b) * a.dkv_rows + pj - a.dkv_row0) * a.dkv_heads +
+                            a.dkv_head0 + kvl) * kD;
       const bool store = key_ok && pj < a.S;
 #pragma unroll
       for (int c = 0; c < kD / 32; ++c) {

@@ -59,8 +59,13 @@ struct BwdArgs {
   const float* lse2;             // [B*hc][S_pad] -LSE * log2(e)
   const float* dvec;             // [B*hc][S_pad] -scale * D_i,  D_i = <dO_i, O_i>
   float* dqacc;                  // [B*hc][S_pad][D] fp32 dQ accumulator
-  void* dk;                      // [B,S,Hkv,D] bf16
-  void* dv;                      // [B,S,Hkv,D] bf16
+  // dK / dV rows: element (b, key position p, kv-head kvl of the group, d) is written at
+  // ((b * dkv_rows + p - dkv_row0) * dkv_heads + dkv_head0 + kvl) * D: the token-major outputs
+  // [B,S,Hkv,D] (rows S, row0 0, heads Hkv, head0 kvh0) or a trunk slot [B,Tn,kc,D].
+  void* dk;
+  void* dv;
+  int64_t dkv_rows, dkv_row0;
+  int dkv_heads, dkv_head0;
   uint32_t* err;
 };
 

@@ -68,7 +68,9 @@ enum { UPIPE_PASS_FWD = 0, UPIPE_PASS_BWD = 1, UPIPE_PASS_BOTH = 2 };
  * unchunked one at the same seq_trunk - the activation-memory cut UPipe reports (UPipe
  * abstract, arXiv 2602.21196: up to 87.5% for a 32B model, i.e. 8 of 64 heads).
  *   pass: UPIPE_PASS_FWD, UPIPE_PASS_BWD or UPIPE_PASS_BOTH (the max of the two).
- *   kv_on_host: 1 if k/v will be pinned host memory (two trunk slots instead of full K/V).
+ *   kv_on_host: 1 if k/v will be pinned host memory (two trunk slots instead of full K/V;
+ *     the backward also reserves two dK and two dV trunk slots, used when dk/dv are pinned
+ *     host memory as well).
  */
 size_t upipe_workspace_bytes(int B, int64_t S, int Hq, int Hkv, int D, int causal,
                              int head_chunk, int64_t seq_trunk, int pass, int kv_on_host);
@@ -92,10 +94,17 @@ int upipe_attn_fwd(const void* q, const void* k, const void* v, void* o, float* 
 
 /*
  * Backward: given the forward's o and lse and the upstream gradient dout, writes
- * dq [B,S,Hq,D], dk and dv [B,S,Hkv,D] (bf16, device; fully overwritten).
+ * dq [B,S,Hq,D], dk and dv [B,S,Hkv,D] (bf16; fully overwritten).
  * P is recomputed from lse (no S x S tensor is stored), D_i = <dout_i, o_i> is formed by a
  * pre-kernel, dq accumulates in a float32 workspace buffer and is converted at the end.
  * Same argument rules as upipe_attn_fwd; workspace sized with UPIPE_PASS_BWD.
+ *   dk, dv: device memory; or, when k and v are pinned host memory, both may be pinned host
+ *     memory too. Then each key/value trunk's dK/dV (final once its launch ends: the backward
+ *     walks key/value trunks outermost) is written to a device slot and copied to the host on
+ *     the library's copy stream while the next trunk computes, so no S-sized key/value tensor
+ *     lives on the device ("Training Ultra Long Context LM with Fully Pipelined Distributed
+ *     Transformer", Key Findings: offloading to host memory with double buffering). The
+ *     caller's stream completes only after the last copy; mixed placement is INVALID_ARG.
  */
 int upipe_attn_bwd(const void* q, const void* k, const void* v, const void* o,
                    const float* lse, const void* dout, void* dq, void* dk, void* dv,

@@ -48,7 +48,10 @@ def _expected_ws(B, S, Hq, Hkv, D, hc, T, kv_host):
     fwd = al(qw) + kv
     if ntr > 1:
         fwd += al(B * hc * T_pad * D * 4) + al(B * hc * T_pad * 8)
-    bwd = 2 * al(qw) + kv + al(B * hc * S_pad * D * 4) + 2 * al(B * hc * S_pad * 4)
+    # host K/V: the backward also holds two dK and two dV trunk slots (used when dk/dv are
+    # pinned host memory as well)
+    dkdv = 4 * al(B * kc * T * D * 2) if kv_host else 0
+    bwd = 2 * al(qw) + kv + dkdv + al(B * hc * S_pad * D * 4) + 2 * al(B * hc * S_pad * 4)
     return fwd, bwd
 
 

@@ -96,6 +96,50 @@ def test_host_kv_equals_device_kv_forward():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+@pytest.mark.parametrize("D,T", [(128, 512), (64, 384)])
+def test_host_dkdv_equals_device_dkdv(D, T):
+    """With K/V and dK/dV all in pinned host memory, each trunk's dK/dV is copied out of a
+    device slot as the next trunk computes. dK/dV accumulate in the same order as in the
+    device run, so they are bitwise identical; dQ (reduced with atomics) is checked against
+    the oracle."""
+    w = WORKLOADS["llama8b_s8k"].with_(S=1400, D=D, Hq=8, Hkv=2, seed=37)
+    q, k, v, do = make_inputs(w, "cpu")
+    qg, dog = q.cuda(), do.cuda()
+    o, lse = up.attention_forward(qg, k.cuda(), v.cuda(), causal=True, head_chunk=4, seq_trunk=T)
+    _, dk1, dv1 = up.attention_backward(qg, k.cuda(), v.cuda(), o, lse, dog, causal=True,
+                                        head_chunk=4, seq_trunk=T)
+    dq2, dk2, dv2 = up.attention_backward(qg, pinned_copy(k), pinned_copy(v), o, lse, dog,
+                                          causal=True, head_chunk=4, seq_trunk=T,
+                                          dkdv_on_host=True)
+    up.upipe_sync_status()
+    assert not dk2.is_cuda and dk2.is_pinned()
+    assert torch.equal(dk1.cpu(), dk2) and torch.equal(dv1.cpu(), dv2)
+    ref = oracle.attn_bwd_ref(*(t.double().numpy() for t in (q, k, v, do)), causal=True)
+    check_full((o, lse, dq2, dk2, dv2), ref, "host dk/dv")
+
+
+def test_host_dkdv_needs_host_kv_and_matching_placement():
+    w = WORKLOADS["mha_s512_d64"]
+    q, k, v, do = (t.cuda() for t in make_inputs(w, "cpu"))
+    o, lse = up.attention_forward(q, k, v)
+    up.upipe_sync_status()
+    B, S, H, D = q.shape
+    dq = torch.empty_like(q)
+    hk = torch.empty((B, S, H, D), dtype=q.dtype, pin_memory=True)
+    dv_dev = torch.empty_like(k)
+    ws = torch.empty(up.upipe_workspace_bytes(B, S, H, H, D, 1, H, S, up.UPIPE_PASS_BWD, 1),
+                     dtype=torch.uint8, device="cuda")
+    n0 = up.upipe_launch_count()
+    for kk, vv, dk_, dv_ in ((k, v, hk, dv_dev),          # mixed dk/dv placement
+                             (k, v, hk, hk.clone().pin_memory()),  # host dk/dv, device k/v
+                             (pinned_copy(k.cpu()), pinned_copy(v.cpu()), hk, dv_dev)):
+        with pytest.raises(up.UpipeError) as ei:
+            up.upipe_attn_bwd(q, kk, vv, o, lse, do, dq, dk_, dv_, B, S, H, H, D, 1, H, S, ws,
+                              None)
+        assert ei.value.status == up.UPIPE_ERR_INVALID_ARG
+    assert up.upipe_launch_count() == n0
+
+
 def test_forward_is_deterministic():
     w = WORKLOADS["llama8b_s8k"].with_(S=1024, seed=34)
     q, k, v, _ = (t.cuda() for t in make_inputs(w, "cpu"))
