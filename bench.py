@@ -65,8 +65,8 @@ def _args():
 TRAFFIC = {
     "attn_bwd": {"workload": "llama8b_s128k", "head_chunk": 8, "seq_trunk": 131072,
                  "files": ["context_parallelism_gb300/csrc/attn_bwd_pp.cu"],
-                 "sha256": "13297857ea532137503734579e763afd5925a5f22e24e4aa498b38d42ada3cc5",
-                 "bytes": 4340129280 + 2160602880},
+                 "sha256": "eb994dca952418e0a92e60ddf9e70bbfef7adc4baa8569ba93222eab89ffef3f",
+                 "bytes": 4325533440 + 2159019008},
     "attn_fwd": {"workload": "llama8b_s128k", "head_chunk": 8, "seq_trunk": 131072,
                  "files": ["context_parallelism_gb300/csrc/attn_fwd_pp.cu"],
                  "sha256": "16c044125171ac7d11a60e4011427ddfd417144aab83888fe40383459cb4c49d",

@@ -209,16 +209,17 @@ def _dims(q, k):
 
 
 def attention_forward(q, k, v, causal=True, head_chunk=None, seq_trunk=None, workspace=None,
-                      stream=None):
+                      stream=None, with_lse=True):
     """o, lse = attention over token-major bf16 q [B,S,Hq,D], k/v [B,S,Hkv,D].
-    k/v may be pinned host tensors (staged trunk by trunk)."""
+    k/v may be pinned host tensors (staged trunk by trunk). with_lse=False is the prefill
+    (inference) form: lse is neither allocated nor written and None is returned for it."""
     import torch
     B, S, Hq, Hkv, D = _dims(q, k)
     hc = head_chunk or Hq
     T = seq_trunk or S
     kv_host = not k.is_cuda
     o = torch.empty_like(q)
-    lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device) if with_lse else None
     need = upipe_workspace_bytes(B, S, Hq, Hkv, D, causal, hc, T, UPIPE_PASS_FWD, kv_host)
     if need == 0:
         upipe_attn_fwd(q, k, v, o, lse, B, S, Hq, Hkv, D, causal, hc, T, 0, 0, stream)

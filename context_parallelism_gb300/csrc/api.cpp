@@ -394,7 +394,8 @@ int upipe_attn_fwd(const void* q, const void* k, const void* v, void* o, float* 
                    int64_t S, int Hq, int Hkv, int D, int causal, int head_chunk,
                    int64_t seq_trunk, void* workspace, size_t workspace_bytes, void* stream_) {
   g_last_error.clear();
-  if (!q || !k || !v || !o || !lse || !workspace)
+  // lse may be NULL: a prefill (inference) forward that keeps no statistics for a backward
+  if (!q || !k || !v || !o || !workspace)
     return fail(UPIPE_ERR_INVALID_ARG, "null pointer argument");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return fail(UPIPE_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
@@ -403,11 +404,11 @@ int upipe_attn_fwd(const void* q, const void* k, const void* v, void* o, float* 
   Plan p0;
   int st = make_plan(B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk, 0, &p0);
   if (st != UPIPE_OK) return st;
-  const void* dptrs[4] = {q, o, lse, workspace};
-  const char* names[4] = {"q", "o", "lse", "workspace"};
+  const void* dptrs[4] = {q, o, workspace, lse};
+  const char* names[4] = {"q", "o", "workspace", "lse"};
   bool kv_host = false;
   int dev = 0;
-  st = check_placement(dptrs, 4, names, k, v, &kv_host, &dev);
+  st = check_placement(dptrs, lse ? 4 : 3, names, k, v, &kv_host, &dev);
   if (st != UPIPE_OK) return st;
   Plan p;
   make_plan(B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk, kv_host ? 1 : 0, &p);

@@ -338,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
           }
         }
-        if (row_ok)
+        if (row_ok && a.lse)  // no LSE in prefill (inference) calls
           a.lse[(static_cast<int64_t>(b) * a.Hq + a.h0 + hl) * a.S + qrow] =
               (m_used + __log2f(l_sum)) * 0.69314718055994530942f;
       } else {

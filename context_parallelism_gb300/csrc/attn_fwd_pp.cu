@@ -359,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   pack_bf16(__uint_as_float(r[8 * i + 6]) * inv_l, __uint_as_float(r[8 * i + 7]) * inv_l));
           }
         }
-        if (row_ok)
+        if (row_ok && a.lse)  // no LSE in prefill (inference) calls
           a.lse[(static_cast<int64_t>(b) * a.Hq + a.h0 + hl) * a.S + qrow] =
               (m_used + __log2f(l_sum)) * 0.69314718055994530942f;
       } else if (srow < a.state_rows) {

@@ -78,7 +78,9 @@ size_t upipe_workspace_bytes(int B, int64_t S, int Hq, int Hkv, int D, int causa
 /*
  * Forward: o = softmax(scale q k^T + mask) v, lse = ln(sum exp(...)).
  *   q [B,S,Hq,D] bf16 (device); k, v [B,S,Hkv,D] bf16 (device, or both pinned host);
- *   o [B,S,Hq,D] bf16 (device, written); lse [B,Hq,S] float32 (device, written).
+ *   o [B,S,Hq,D] bf16 (device, written); lse [B,Hq,S] float32 (device, written), or NULL
+ *     for a prefill (inference) call that keeps no softmax statistics: then only o is
+ *     written, by the same kernels.
  *   causal: 1 = key j visible to query i iff j <= i; 0 = full attention.
  *   head_chunk: q-heads per group; must divide Hq and be a multiple of Hq/Hkv (a group owns
  *     whole kv-heads). head_chunk = Hq is the unchunked schedule.

@@ -140,6 +140,21 @@ def test_host_dkdv_needs_host_kv_and_matching_placement():
     assert up.upipe_launch_count() == n0
 
 
+@pytest.mark.parametrize("D,host_kv", [(128, False), (128, True), (64, False)])
+def test_prefill_forward_without_lse(D, host_kv):
+    """A prefill (inference) forward passes no lse buffer: the same kernels run, only o is
+    written, and it is bitwise the o of the training forward (several trunks, ragged tail)."""
+    w = WORKLOADS["llama8b_s8k"].with_(S=1100, D=D, Hq=8, Hkv=2, seed=38)
+    q, k, v, _ = make_inputs(w, "cpu")
+    qg = q.cuda()
+    kk, vv = (pinned_copy(k), pinned_copy(v)) if host_kv else (k.cuda(), v.cuda())
+    o1, _ = up.attention_forward(qg, kk, vv, causal=True, head_chunk=4, seq_trunk=256)
+    o2, l2 = up.attention_forward(qg, kk, vv, causal=True, head_chunk=4, seq_trunk=256,
+                                  with_lse=False)
+    up.upipe_sync_status()
+    assert l2 is None and torch.equal(o1, o2)
+
+
 def test_forward_is_deterministic():
     w = WORKLOADS["llama8b_s8k"].with_(S=1024, seed=34)
     q, k, v, _ = (t.cuda() for t in make_inputs(w, "cpu"))
