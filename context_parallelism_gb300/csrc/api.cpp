@@ -235,8 +235,12 @@ int make_plan(int B, int64_t S, int Hq, int Hkv, int D, int causal, int head_chu
     p->f_vw = take(kvw);
   }
   if (p->n_trunks > 1) {
-    p->f_state_o = take(hcB * p->T_pad * D * 4);
-    p->f_state_ml = take(hcB * p->T_pad * 2 * 4);
+    // Host K/V: the forward walks key/value trunks outermost (each trunk is staged once), so
+    // the running state of every query trunk is kept: S_pad rows. Device K/V: one query
+    // trunk at a time, T_pad rows.
+    const int64_t rows = p->kv_host ? p->S_pad : p->T_pad;
+    p->f_state_o = take(hcB * rows * D * 4);
+    p->f_state_ml = take(hcB * rows * 2 * 4);
   }
   p->f_total = off;
   // backward
@@ -431,13 +435,37 @@ int upipe_attn_fwd(const void* q, const void* k, const void* v, void* o, float* 
   Stager stg{p, ds, stream, k, v, {ws + p.f_slot_k[0], ws + p.f_slot_k[1]},
              {ws + p.f_slot_v[0], ws + p.f_slot_v[1]}, {}, 0};
   if (kv_host) {
+    // one staging job per (group, key/value trunk): the trunk serves every query trunk
     for (int g = 0; g < Hq / p.hc; ++g)
-      for (int m = 0; m < p.n_trunks; ++m)
-        for (int n = 0; n <= (causal ? m : p.n_trunks - 1); ++n) stg.jobs.push_back({g * p.kc, n});
+      for (int n = 0; n < p.n_trunks; ++n) stg.jobs.push_back({g * p.kc, n});
     // The copy stream must not touch the workspace before earlier work on `stream` is done.
     UPIPE_CUDA(cudaEventRecord(ds->entry, stream));
     UPIPE_CUDA(cudaStreamWaitEvent(ds->copy, ds->entry, 0));
   }
+  auto launch = [&](const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, int h0,
+                    int m, int n, int64_t row_lo, int64_t row_hi, int64_t pos0,
+                    int64_t state_stride) -> int {
+    const int n_last = causal ? m : p.n_trunks - 1;
+    FwdArgs a{};
+    a.q_lo = static_cast<int64_t>(m) * p.T;
+    a.q_hi = std::min<int64_t>(S, a.q_lo + p.T);
+    a.S = S;
+    a.hc = p.hc; a.kc = p.kc; a.G = p.G; a.Hq = Hq; a.h0 = h0;
+    a.causal = causal; a.first = (n == 0); a.last = (n == n_last);
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.o = o; a.lse = lse;
+    // with an S-sized state the rows of query trunk m start m*T rows in
+    const int64_t soff = state_stride ? a.q_lo : 0;
+    a.state_o = state_o ? state_o + soff * D : nullptr;
+    a.state_ml = state_ml ? state_ml + soff * 2 : nullptr;
+    // rows past the state buffer's end are never written (the last trunk may be ragged)
+    a.state_rows = state_stride ? std::min<int64_t>(p.T_pad, p.S_pad - a.q_lo) : p.T_pad;
+    a.state_stride = state_stride;
+    a.err = ds->err;
+    a.kv_row_lo = row_lo; a.kv_row_hi = row_hi; a.kv_pos0 = pos0;
+    UPIPE_CUDA(launch_attn_fwd(D, B, tq, tk, tv, a, stream));
+    return UPIPE_OK;
+  };
   int job = 0;
   for (int g = 0; g < Hq / p.hc; ++g) {
     const int h0 = g * p.hc, kvh0 = g * p.kc;
@@ -449,40 +477,35 @@ int upipe_attn_fwd(const void* q, const void* k, const void* v, void* o, float* 
     CUtensorMap tq, tk, tv;
     UPIPE_CUDA(make_tmap_bf16(&tq, qw, D, S, static_cast<int64_t>(B) * p.hc));
     if (!kv_host) {
+      // FPDT order: query trunk m folds key/value trunks 0..m into a T-row state
       UPIPE_CUDA(make_tmap_bf16(&tk, ws + p.f_kw, D, S, static_cast<int64_t>(B) * p.kc));
       UPIPE_CUDA(make_tmap_bf16(&tv, ws + p.f_vw, D, S, static_cast<int64_t>(B) * p.kc));
-    }
-    for (int m = 0; m < p.n_trunks; ++m) {
-      const int64_t q_lo = static_cast<int64_t>(m) * p.T;
-      const int64_t q_hi = std::min<int64_t>(S, q_lo + p.T);
-      const int n_last = causal ? m : p.n_trunks - 1;
-      for (int n = 0; n <= n_last; ++n, ++job) {
-        const int64_t t0 = static_cast<int64_t>(n) * p.T;
-        const int64_t Tn = std::min<int64_t>(p.T, S - t0);
-        FwdArgs a{};
-        a.q_lo = q_lo; a.q_hi = q_hi; a.S = S;
-        a.hc = p.hc; a.kc = p.kc; a.G = p.G; a.Hq = Hq; a.h0 = h0;
-        a.causal = causal; a.first = (n == 0); a.last = (n == n_last);
-        a.scale_log2 = scale * 1.4426950408889634f;
-        a.o = o; a.lse = lse;
-        a.state_o = state_o; a.state_ml = state_ml; a.state_rows = p.T_pad;
-        a.err = ds->err;
-        if (kv_host) {
-          st = stg.before(job);
-          if (st != UPIPE_OK) return st;
-          const int s = job & 1;
-          UPIPE_CUDA(make_tmap_bf16(&tk, stg.slot_k[s], D, Tn, static_cast<int64_t>(B) * p.kc));
-          UPIPE_CUDA(make_tmap_bf16(&tv, stg.slot_v[s], D, Tn, static_cast<int64_t>(B) * p.kc));
-          a.kv_row_lo = 0; a.kv_row_hi = Tn; a.kv_pos0 = t0;
-        } else {
-          a.kv_row_lo = t0; a.kv_row_hi = t0 + Tn; a.kv_pos0 = 0;
-        }
-        UPIPE_CUDA(launch_attn_fwd(D, B, tq, tk, tv, a, stream));
-        if (kv_host) {
-          st = stg.after(job);
+      for (int m = 0; m < p.n_trunks; ++m) {
+        const int n_last = causal ? m : p.n_trunks - 1;
+        for (int n = 0; n <= n_last; ++n) {
+          const int64_t t0 = static_cast<int64_t>(n) * p.T;
+          st = launch(tq, tk, tv, h0, m, n, t0, std::min<int64_t>(S, t0 + p.T), 0, 0);
           if (st != UPIPE_OK) return st;
         }
       }
+      continue;
+    }
+    // Host K/V: key/value trunk n is staged once and then met by every query trunk that sees
+    // it (m >= n when causal); each query trunk keeps its running state in an S-sized buffer.
+    for (int n = 0; n < p.n_trunks; ++n, ++job) {
+      const int64_t t0 = static_cast<int64_t>(n) * p.T;
+      const int64_t Tn = std::min<int64_t>(p.T, S - t0);
+      st = stg.before(job);
+      if (st != UPIPE_OK) return st;
+      const int s = job & 1;
+      UPIPE_CUDA(make_tmap_bf16(&tk, stg.slot_k[s], D, Tn, static_cast<int64_t>(B) * p.kc));
+      UPIPE_CUDA(make_tmap_bf16(&tv, stg.slot_v[s], D, Tn, static_cast<int64_t>(B) * p.kc));
+      for (int m = causal ? n : 0; m < p.n_trunks; ++m) {
+        st = launch(tq, tk, tv, h0, m, n, 0, Tn, t0, p.n_trunks > 1 ? p.S_pad : 0);
+        if (st != UPIPE_OK) return st;
+      }
+      st = stg.after(job);
+      if (st != UPIPE_OK) return st;
     }
   }
   return UPIPE_OK;

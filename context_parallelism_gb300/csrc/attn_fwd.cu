@@ -210,10 +210,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     const int64_t qrow = q0 + t;
     const int64_t srow = (q0 - a.q_lo) + t;  // row inside the carried state
+    const int64_t sstride = a.state_stride ? a.state_stride : a.state_rows;
     float m_used = -INFINITY;  // log2 units
     float l_sum = 0.f;
     if (!a.first) {
-      const float* so = a.state_o + (static_cast<int64_t>(zq) * a.state_rows + srow) * D;
+      const float* so = a.state_o + (static_cast<int64_t>(zq) * sstride + srow) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
@@ -229,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_wait_st();
       const float2 ml =
-          *reinterpret_cast<const float2*>(a.state_ml + (static_cast<int64_t>(zq) * a.state_rows + srow) * 2);
+          *reinterpret_cast<const float2*>(a.state_ml + (static_cast<int64_t>(zq) * sstride + srow) * 2);
       m_used = ml.x;
       l_sum = ml.y;
     }
@@ -342,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           a.lse[(static_cast<int64_t>(b) * a.Hq + a.h0 + hl) * a.S + qrow] =
               (m_used + __log2f(l_sum)) * 0.69314718055994530942f;
       } else {
-        float* so = a.state_o + (static_cast<int64_t>(zq) * a.state_rows + srow) * D;
+        float* so = a.state_o + (static_cast<int64_t>(zq) * sstride + srow) * D;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
@@ -353,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
                             __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
         }
-        *reinterpret_cast<float2*>(a.state_ml + (static_cast<int64_t>(zq) * a.state_rows + srow) * 2) =
+        *reinterpret_cast<float2*>(a.state_ml + (static_cast<int64_t>(zq) * sstride + srow) * 2) =
             make_float2(m_used, l_sum);
       }
     }

@@ -208,12 +208,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t qw0 = q0 + 128 * w;
     const int64_t qrow = qw0 + t;
     const int64_t srow = (qw0 - a.q_lo) + t;  // row inside the carried state
+    const int64_t sstride = a.state_stride ? a.state_stride : a.state_rows;
     float m_used = -INFINITY;  // log2 units
     float l_sum = 0.f;
     // Rows past the carried state (the second tile of a trunk with an odd tile count) belong
     // to no output; they compute on whatever TMEM holds and are never stored.
     if (!a.first && srow < a.state_rows) {
-      const float* so = a.state_o + (static_cast<int64_t>(zq) * a.state_rows + srow) * kD;
+      const float* so = a.state_o + (static_cast<int64_t>(zq) * sstride + srow) * kD;
 #pragma unroll
       for (int c = 0; c < kD / 32; ++c) {
         uint32_t r[32];
@@ -229,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_wait_st();
       const float2 ml = *reinterpret_cast<const float2*>(
-          a.state_ml + (static_cast<int64_t>(zq) * a.state_rows + srow) * 2);
+          a.state_ml + (static_cast<int64_t>(zq) * sstride + srow) * 2);
       m_used = ml.x;
       l_sum = ml.y;
     }
@@ -363,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           a.lse[(static_cast<int64_t>(b) * a.Hq + a.h0 + hl) * a.S + qrow] =
               (m_used + __log2f(l_sum)) * 0.69314718055994530942f;
       } else if (srow < a.state_rows) {
-        float* so = a.state_o + (static_cast<int64_t>(zq) * a.state_rows + srow) * kD;
+        float* so = a.state_o + (static_cast<int64_t>(zq) * sstride + srow) * kD;
 #pragma unroll
         for (int c = 0; c < kD / 32; ++c) {
           uint32_t r[32];
@@ -374,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
                             __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
         }
-        *reinterpret_cast<float2*>(a.state_ml + (static_cast<int64_t>(zq) * a.state_rows + srow) * 2) =
+        *reinterpret_cast<float2*>(a.state_ml + (static_cast<int64_t>(zq) * sstride + srow) * 2) =
             make_float2(m_used, l_sum);
       }
     }

@@ -35,9 +35,10 @@ struct FwdArgs {
   float scale_log2;              // softmax scale * log2(e)
   void* o;                       // [B,S,Hq,D] bf16, written when last
   float* lse;                    // [B,Hq,S], written when last
-  float* state_o;                // [B*hc][state_rows][D] fp32 running numerator (rows from q_lo)
-  float* state_ml;               // [B*hc][state_rows][2] fp32 running max (log2 units), sum
-  int64_t state_rows;
+  float* state_o;                // [B*hc][state_stride][D] fp32 running numerator (rows from q_lo)
+  float* state_ml;               // [B*hc][state_stride][2] fp32 running max (log2 units), sum
+  int64_t state_rows;            // rows of this launch's state (rows past it are never stored)
+  int64_t state_stride;          // rows per head in the state buffers; 0 means state_rows
   uint32_t* err;                 // device status word
 };
 

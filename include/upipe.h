@@ -69,8 +69,10 @@ enum { UPIPE_PASS_FWD = 0, UPIPE_PASS_BWD = 1, UPIPE_PASS_BOTH = 2 };
  * abstract, arXiv 2602.21196: up to 87.5% for a 32B model, i.e. 8 of 64 heads).
  *   pass: UPIPE_PASS_FWD, UPIPE_PASS_BWD or UPIPE_PASS_BOTH (the max of the two).
  *   kv_on_host: 1 if k/v will be pinned host memory (two trunk slots instead of full K/V;
- *     the backward also reserves two dK and two dV trunk slots, used when dk/dv are pinned
- *     host memory as well).
+ *     the forward then walks key/value trunks outermost, staging each once, and keeps every
+ *     query trunk's fp32 running state: head_chunk*S*(D+2)*4 bytes per batch row; the
+ *     backward also reserves two dK and two dV trunk slots, used when dk/dv are pinned host
+ *     memory as well).
  */
 size_t upipe_workspace_bytes(int B, int64_t S, int Hq, int Hkv, int D, int causal,
                              int head_chunk, int64_t seq_trunk, int pass, int kv_on_host);

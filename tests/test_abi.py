@@ -46,8 +46,9 @@ def _expected_ws(B, S, Hq, Hkv, D, hc, T, kv_host):
     qw = B * hc * S * D * 2
     kv = 4 * al(B * kc * T * D * 2) if kv_host else 2 * al(B * kc * S * D * 2)
     fwd = al(qw) + kv
-    if ntr > 1:
-        fwd += al(B * hc * T_pad * D * 4) + al(B * hc * T_pad * 8)
+    if ntr > 1:  # running state: every query trunk's rows with host K/V, one trunk's otherwise
+        rows = S_pad if kv_host else T_pad
+        fwd += al(B * hc * rows * D * 4) + al(B * hc * rows * 8)
     # host K/V: the backward also holds two dK and two dV trunk slots (used when dk/dv are
     # pinned host memory as well)
     dkdv = 4 * al(B * kc * T * D * 2) if kv_host else 0
