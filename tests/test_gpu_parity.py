@@ -39,6 +39,8 @@ CASES = [
     (1, 129, 4, 2, 64, True, 2, 128, False),     # one full tile + 1-row tail
     (1, 1, 2, 1, 128, True, 2, 1, False),        # a single token
     (3, 300, 6, 3, 128, False, 6, 300, False),   # odd head counts, non-causal
+    (1, 900, 8, 2, 128, False, 4, 256, True),    # host K/V, non-causal: every trunk pair
+    (2, 700, 4, 2, 64, True, 2, 256, True),      # host K/V, D = 64, batch 2, ragged
 ]
 
 
