@@ -69,8 +69,8 @@ TRAFFIC = {
                  "bytes": 4325533440 + 2159019008},
     "attn_fwd": {"workload": "llama8b_s128k", "head_chunk": 8, "seq_trunk": 131072,
                  "files": ["context_parallelism_gb300/csrc/attn_fwd_pp.cu"],
-                 "sha256": "16c044125171ac7d11a60e4011427ddfd417144aab83888fe40383459cb4c49d",
-                 "bytes": 917466624 + 255216896},
+                 "sha256": "0fc8f248f8edfa9bb850c818a8d0491a4d0934cced9ead929024e61b5c60f791",
+                 "bytes": 919404288 + 255160320},
 }
 
 

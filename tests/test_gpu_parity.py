@@ -157,6 +157,26 @@ def test_prefill_forward_without_lse(D, host_kv):
     assert l2 is None and torch.equal(o1, o2)
 
 
+def test_rising_scores_force_rescales():
+    """The last head-dim channel carries a ramp: q's is 2 and key j's is 0.28*j, so every
+    score rises by about 0.05 per key (on top of the random part). The row maximum then climbs
+    by ~9 log2 units per 128-key tile, so the forward's running maximum moves in nearly every
+    tile, also between the two 64-column halves (the exact power-of-two rescale of O, the row
+    sum and the first half's P), while each row's softmax stays ~20 keys wide."""
+    w = WORKLOADS["llama8b_s8k"].with_(S=1536, Hq=8, Hkv=2, seed=39)
+    q, k, v, do = make_inputs(w, "cpu")
+    q[..., -1] = 2.0
+    k[..., -1] = (0.28 * torch.arange(w.S, dtype=torch.float32)).view(1, w.S, 1).to(torch.bfloat16)
+    ref = _oracle(q, k, v, do, True)
+    o, lse, dq, dk, dv = gpu_fwd_bwd(q.cuda(), k.cuda(), v.cuda(), do.cuda(), True, 4, 512)
+    # dQ's ramp channel is sum_j dS_ij * 0.28 j with sum_j dS_ij = 0: rounding dS to bf16 for
+    # the dQ MMA (as any bf16 attention backward does) leaves ~3 % there even with everything
+    # else exact, so that one channel is left out of the dQ check.
+    dq_ref = ref[2][..., :-1]
+    check_full((o, lse, dq[..., :-1], dk, dv), (ref[0], ref[1], dq_ref, ref[3], ref[4]),
+               "rising scores")
+
+
 def test_forward_is_deterministic():
     w = WORKLOADS["llama8b_s8k"].with_(S=1024, seed=34)
     q, k, v, _ = (t.cuda() for t in make_inputs(w, "cpu"))
