@@ -349,6 +349,20 @@ def run_ours(a):
                     "unit": "GB/s", "frac": None, "traffic": None}
     kernels = {kname: {"ms_per_step": t / a.steps, "launches_per_step": n / a.steps}
                for kname, (t, n) in prof.items() if n}
+    # HBM-bound kernels against the measured copy bandwidth: algorithmic bytes per step (each
+    # element read and written once) over their summed event time.
+    elem_q = B * S * Hq * D
+    elem_kv = 0 if kv_host else 2 * B * S * Hkv * D
+    hbm_bytes = {
+        "layout": 2 * 2 * 2 * (elem_q + elem_kv),  # fwd + bwd gathers, bf16 read + write
+        "bwd_pre": elem_q * (2 + 2 + 2 + 4),        # read O, dO; write dO gather, zero dQ acc
+        "dq_convert": elem_q * (4 + 2),             # read fp32 dQ acc, write bf16 dQ
+    }
+    for kname, nbytes in hbm_bytes.items():
+        if kname in kernels and kernels[kname]["ms_per_step"] > 0:
+            gbs = nbytes / (kernels[kname]["ms_per_step"] / 1e3) / 1e9
+            kernels[kname].update({"algorithmic_gb_per_step": nbytes / 1e9, "gbs": gbs,
+                                   "frac_of_hbm": gbs / float(peaks["hbm_gbs"])})
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
@@ -382,38 +396,52 @@ def run_ours(a):
         h2d = hq.nbytes + hdo.nbytes + (0 if kv_host else hk.nbytes + hv.nbytes)
         d2h = sum(t.nbytes for t in outs_h)
 
-        def e2e_step():
+        # The step a user would write: dO is copied in on a side stream while the forward
+        # runs (only the backward reads it), and O and LSE are copied out on that stream while
+        # the backward runs; q, k, v in and dQ, dK, dV out sit on the compute stream.
+        side = torch.cuda.Stream(dev)
+        ev_start = torch.cuda.Event()
+        ev_do = torch.cuda.Event()
+        ev_fwd = torch.cuda.Event()
+        ev_out = torch.cuda.Event()
+
+        def e2e_step_marked(evs=None):
+            if evs:
+                evs[0].record(stream)
+            ev_start.record(stream)
+            side.wait_event(ev_start)
+            with torch.cuda.stream(side):
+                do.copy_(hdo, non_blocking=True)
+            ev_do.record(side)
             q.copy_(hq, non_blocking=True)
-            do.copy_(hdo, non_blocking=True)
             if not kv_host:
                 k_in.copy_(hk, non_blocking=True)
                 v_in.copy_(hv, non_blocking=True)
+            if evs:
+                evs[1].record(stream)
             up.upipe_attn_fwd(q, k_in, v_in, o, lse, B, S, Hq, Hkv, D, 1, hc, T, ws, ws_bytes, stream)
+            ev_fwd.record(stream)
+            side.wait_event(ev_fwd)
+            with torch.cuda.stream(side):
+                outs_h[0].copy_(o, non_blocking=True)
+                outs_h[1].copy_(lse, non_blocking=True)
+            ev_out.record(side)
+            stream.wait_event(ev_do)
             up.upipe_attn_bwd(q, k_in, v_in, o, lse, do, dq, dk, dv, B, S, Hq, Hkv, D, 1, hc, T,
                               ws, ws_bytes, stream)
-            for hdst, dsrc in zip(outs_h, (o, lse, dq, dk, dv)):
+            if evs:
+                evs[2].record(stream)
+            for hdst, dsrc in zip(outs_h[2:], (dq, dk, dv)):
                 hdst.copy_(dsrc, non_blocking=True)
+            # the next step overwrites o/lse: their copy-out must be done (and so must this one)
+            stream.wait_event(ev_out)
+            if evs:
+                evs[3].record(stream)
 
-        e2e_step()
+        e2e_step_marked()
         barrier()
         # per-phase events (host->device, compute, device->host) of the same steps
         ph = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(a.steps)]
-
-        def e2e_step_marked(evs):
-            evs[0].record(stream)
-            q.copy_(hq, non_blocking=True)
-            do.copy_(hdo, non_blocking=True)
-            if not kv_host:
-                k_in.copy_(hk, non_blocking=True)
-                v_in.copy_(hv, non_blocking=True)
-            evs[1].record(stream)
-            up.upipe_attn_fwd(q, k_in, v_in, o, lse, B, S, Hq, Hkv, D, 1, hc, T, ws, ws_bytes, stream)
-            up.upipe_attn_bwd(q, k_in, v_in, o, lse, do, dq, dk, dv, B, S, Hq, Hkv, D, 1, hc, T,
-                              ws, ws_bytes, stream)
-            evs[2].record(stream)
-            for hdst, dsrc in zip(outs_h, (o, lse, dq, dk, dv)):
-                hdst.copy_(dsrc, non_blocking=True)
-            evs[3].record(stream)
 
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
@@ -426,7 +454,8 @@ def run_ours(a):
                      for i, k in enumerate(("h2d_ms", "compute_ms", "d2h_ms"))}
         e2e_value, _ = job_throughput(e0.elapsed_time(e1), a.steps, f_fwd + f_bwd, world, red)
         line["e2e"] = {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-                       "d2h_bytes_per_step": int(d2h), "per_step_ms": breakdown}
+                       "d2h_bytes_per_step": int(d2h), "per_step_ms": breakdown,
+                       "overlap": "dO in during the forward, O and LSE out during the backward"}
         up.upipe_sync_status(stream)
 
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
