@@ -362,29 +362,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                              (r0 + 128 > a.kv_row_hi);
       uint32_t r[64];
       tmem_ld64_sync(tS + lane_off + 64 * w, r);
+      // Two 32-column halves: the first half's bf16 P^T is stored while the second half is
+      // exponentiated, so the store's latency is hidden behind MUFU work.
 #pragma unroll
-      for (int x = 0; x < 64; x += 4) {
-        // -LSE*log2e pairs straight from shared memory as packed fp32x2 operands
-        const ulonglong2 l4 = *reinterpret_cast<const ulonglong2*>(lse_s + x);
-        float y0, y1, y2, y3;
-        f2_unpack(ffma2(f2_pack_u(r[x], r[x + 1]), sl2, l4.x), y0, y1);
-        f2_unpack(ffma2(f2_pack_u(r[x + 2], r[x + 3]), sl2, l4.y), y2, y3);
-        p[x + 0] = ex2_approx(y0);
-        p[x + 1] = ex2_approx(y1);
-        p[x + 2] = ex2_approx(y2);
-        p[x + 3] = ex2_approx(y3);
-      }
-      if (need_mask) {
+      for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const int64_t q = qc0 + c;
-          if (!(key_ok && q < a.S && (!a.causal || q >= pj))) p[c] = 0.f;
+        for (int x = 32 * hh; x < 32 * hh + 32; x += 4) {
+          // -LSE*log2e pairs straight from shared memory as packed fp32x2 operands
+          const ulonglong2 l4 = *reinterpret_cast<const ulonglong2*>(lse_s + x);
+          float y0, y1, y2, y3;
+          f2_unpack(ffma2(f2_pack_u(r[x], r[x + 1]), sl2, l4.x), y0, y1);
+          f2_unpack(ffma2(f2_pack_u(r[x + 2], r[x + 3]), sl2, l4.y), y2, y3);
+          p[x + 0] = ex2_approx(y0);
+          p[x + 1] = ex2_approx(y1);
+          p[x + 2] = ex2_approx(y2);
+          p[x + 3] = ex2_approx(y3);
         }
-      }
-      uint32_t pk[32];
+        if (need_mask) {
 #pragma unroll
-      for (int x = 0; x < 32; ++x) pk[x] = pack_bf16(p[2 * x], p[2 * x + 1]);
-      tmem_st32(tS + lane_off + 64 * w, pk);
+          for (int c = 32 * hh; c < 32 * hh + 32; ++c) {
+            const int64_t q = qc0 + c;
+            if (!(key_ok && q < a.S && (!a.causal || q >= pj))) p[c] = 0.f;
+          }
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) pk[x] = pack_bf16(p[32 * hh + 2 * x], p[32 * hh + 2 * x + 1]);
+        tmem_st16(tS + lane_off + 64 * w + 16 * hh, pk);
+      }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
