@@ -65,8 +65,8 @@ def _args():
 TRAFFIC = {
     "attn_bwd": {"workload": "llama8b_s128k", "head_chunk": 8, "seq_trunk": 131072,
                  "files": ["context_parallelism_gb300/csrc/attn_bwd_pp.cu"],
-                 "sha256": "eb994dca952418e0a92e60ddf9e70bbfef7adc4baa8569ba93222eab89ffef3f",
-                 "bytes": 4325533440 + 2159019008},
+                 "sha256": "6d7d465475a91a26801257865763f35b361536eff2a92e9d7957bd9c27f24b34",
+                 "bytes": 4308017408 + 2163678464},
     "attn_fwd": {"workload": "llama8b_s128k", "head_chunk": 8, "seq_trunk": 131072,
                  "files": ["context_parallelism_gb300/csrc/attn_fwd_pp.cu"],
                  "sha256": "0fc8f248f8edfa9bb850c818a8d0491a4d0934cced9ead929024e61b5c60f791",
