@@ -98,13 +98,13 @@ def test_host_kv_equals_device_kv_forward():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-@pytest.mark.parametrize("D,T", [(128, 512), (64, 384)])
-def test_host_dkdv_equals_device_dkdv(D, T):
+@pytest.mark.parametrize("B,D,T", [(1, 128, 512), (2, 64, 384)])
+def test_host_dkdv_equals_device_dkdv(B, D, T):
     """With K/V and dK/dV all in pinned host memory, each trunk's dK/dV is copied out of a
     device slot as the next trunk computes. dK/dV accumulate in the same order as in the
     device run, so they are bitwise identical; dQ (reduced with atomics) is checked against
     the oracle."""
-    w = WORKLOADS["llama8b_s8k"].with_(S=1400, D=D, Hq=8, Hkv=2, seed=37)
+    w = WORKLOADS["llama8b_s8k"].with_(B=B, S=1400, D=D, Hq=8, Hkv=2, seed=37)
     q, k, v, do = make_inputs(w, "cpu")
     qg, dog = q.cuda(), do.cuda()
     o, lse = up.attention_forward(qg, k.cuda(), v.cuda(), causal=True, head_chunk=4, seq_trunk=T)
