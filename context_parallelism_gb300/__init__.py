@@ -25,6 +25,7 @@ UPIPE_ERR_CUDA = 4
 UPIPE_ERR_TIMEOUT = 5
 
 UPIPE_PASS_FWD, UPIPE_PASS_BWD, UPIPE_PASS_BOTH = 0, 1, 2
+UPIPE_HOST_KV, UPIPE_HOST_ACT = 1, 2
 
 KERNEL_CLASSES = ["layout", "attn_fwd", "bwd_pre", "attn_bwd", "dq_convert", "other"]
 
@@ -110,9 +111,10 @@ def _check(status, where):
 # ---- one-to-one ABI wrappers ------------------------------------------------------------
 
 def upipe_workspace_bytes(B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk, pass_=UPIPE_PASS_BOTH,
-                          kv_on_host=0):
+                          host_mask=0):
+    """host_mask: UPIPE_HOST_KV | UPIPE_HOST_ACT bits (True/1 keeps meaning host k/v)."""
     return int(_lib.upipe_workspace_bytes(B, S, Hq, Hkv, D, int(causal), head_chunk, seq_trunk,
-                                          pass_, int(kv_on_host)))
+                                          pass_, int(host_mask)))
 
 
 def upipe_attn_fwd(q, k, v, o, lse, B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk, workspace,
@@ -120,7 +122,7 @@ def upipe_attn_fwd(q, k, v, o, lse, B, S, Hq, Hkv, D, causal, head_chunk, seq_tr
     wb = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
     st = _lib.upipe_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, S, Hq, Hkv, D,
                              int(causal), head_chunk, seq_trunk, _ptr(workspace), wb,
-                             _stream(stream, q, o))
+                             _stream(stream, q, o, workspace))
     _check(st, "upipe_attn_fwd")
 
 
@@ -129,7 +131,7 @@ def upipe_attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, S, Hq, Hkv, D, causal, 
     wb = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
     st = _lib.upipe_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
                              _ptr(dk), _ptr(dv), B, S, Hq, Hkv, D, int(causal), head_chunk,
-                             seq_trunk, _ptr(workspace), wb, _stream(stream, q, dq))
+                             seq_trunk, _ptr(workspace), wb, _stream(stream, q, dq, lse, workspace))
     _check(st, "upipe_attn_bwd")
 
 
@@ -208,49 +210,72 @@ def _dims(q, k):
     return B, S, Hq, k.shape[2], D
 
 
+def _device_of(*tensors):
+    import torch
+    for t in tensors:
+        if t is not None and t.is_cuda:
+            return t.device
+    return torch.device("cuda", torch.cuda.current_device())
+
+
 def attention_forward(q, k, v, causal=True, head_chunk=None, seq_trunk=None, workspace=None,
-                      stream=None, with_lse=True):
+                      stream=None, with_lse=True, o_on_host=False):
     """o, lse = attention over token-major bf16 q [B,S,Hq,D], k/v [B,S,Hkv,D].
-    k/v may be pinned host tensors (staged trunk by trunk). with_lse=False is the prefill
-    (inference) form: lse is neither allocated nor written and None is returned for it."""
+    q, k/v may be pinned host tensors (staged head group by head group, trunk by trunk);
+    o_on_host returns o as a pinned host tensor, copied out group by group. with_lse=False is
+    the prefill (inference) form: lse is neither allocated nor written and None is returned."""
     import torch
     B, S, Hq, Hkv, D = _dims(q, k)
     hc = head_chunk or Hq
     T = seq_trunk or S
+    dev = _device_of(q, k)
     kv_host = not k.is_cuda
-    o = torch.empty_like(q)
-    lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device) if with_lse else None
-    need = upipe_workspace_bytes(B, S, Hq, Hkv, D, causal, hc, T, UPIPE_PASS_FWD, kv_host)
+    mask = (UPIPE_HOST_KV if kv_host else 0) | (UPIPE_HOST_ACT if (not q.is_cuda or o_on_host)
+                                                else 0)
+    if o_on_host:
+        o = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    else:
+        o = torch.empty(q.shape, dtype=q.dtype, device=dev)
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device=dev) if with_lse else None
+    need = upipe_workspace_bytes(B, S, Hq, Hkv, D, causal, hc, T, UPIPE_PASS_FWD, mask)
     if need == 0:
         upipe_attn_fwd(q, k, v, o, lse, B, S, Hq, Hkv, D, causal, hc, T, 0, 0, stream)
     if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     upipe_attn_fwd(q, k, v, o, lse, B, S, Hq, Hkv, D, causal, hc, T, workspace, None, stream)
     return o, lse
 
 
 def attention_backward(q, k, v, o, lse, dout, causal=True, head_chunk=None, seq_trunk=None,
-                       workspace=None, stream=None, dkdv_on_host=False):
-    """dq, dk, dv for the forward above. dk/dv are device tensors, or pinned host tensors when
-    dkdv_on_host (which needs host k/v): then each trunk's dK/dV is copied out as it finishes."""
+                       workspace=None, stream=None, dkdv_on_host=False, dq_on_host=False):
+    """dq, dk, dv for the forward above. q, o, dout may be pinned host tensors (staged head
+    group by head group); dq_on_host returns dq as a pinned host tensor, copied out group by
+    group. dk/dv are device tensors, or pinned host tensors when dkdv_on_host (which needs host
+    k/v): then each trunk's dK/dV is copied out as it finishes."""
     import torch
     B, S, Hq, Hkv, D = _dims(q, k)
     hc = head_chunk or Hq
     T = seq_trunk or S
+    dev = _device_of(q, k, lse)
     kv_host = not k.is_cuda
-    dq = torch.empty_like(q)
+    act_host = dq_on_host or not (q.is_cuda and o.is_cuda and dout.is_cuda)
+    mask = (UPIPE_HOST_KV if kv_host else 0) | (UPIPE_HOST_ACT if act_host else 0)
+    if dq_on_host:
+        dq = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    else:
+        dq = torch.empty(q.shape, dtype=q.dtype, device=dev)
     if dkdv_on_host:
         dk = torch.empty((B, S, Hkv, D), dtype=q.dtype, pin_memory=True)
         dv = torch.empty((B, S, Hkv, D), dtype=q.dtype, pin_memory=True)
     else:
-        dk = torch.empty((B, S, Hkv, D), dtype=q.dtype, device=q.device)
-        dv = torch.empty((B, S, Hkv, D), dtype=q.dtype, device=q.device)
-    need = upipe_workspace_bytes(B, S, Hq, Hkv, D, causal, hc, T, UPIPE_PASS_BWD, kv_host)
+        dk = torch.empty((B, S, Hkv, D), dtype=q.dtype, device=dev)
+        dv = torch.empty((B, S, Hkv, D), dtype=q.dtype, device=dev)
+    need = upipe_workspace_bytes(B, S, Hq, Hkv, D, causal, hc, T, UPIPE_PASS_BWD, mask)
     if need == 0:
         upipe_attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, S, Hq, Hkv, D, causal, hc, T, 0, 0,
                        stream)
     if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     upipe_attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, S, Hq, Hkv, D, causal, hc, T, workspace,
                    None, stream)
     return dq, dk, dv

@@ -63,6 +63,10 @@ struct DevState {
   cudaEvent_t slot_free[2] = {nullptr, nullptr};
   cudaEvent_t dkdv_done[2] = {nullptr, nullptr};  // a dK/dV slot is written (compute stream)
   cudaEvent_t dkdv_free[2] = {nullptr, nullptr};  // its copy to the host is done (copy stream)
+  cudaEvent_t act_ready[2] = {nullptr, nullptr};  // a group's host activations staged in
+  cudaEvent_t act_free[2] = {nullptr, nullptr};   // the group's kernels are done with them
+  cudaEvent_t out_done[2] = {nullptr, nullptr};   // a group's outputs are in their staging
+  cudaEvent_t out_free[2] = {nullptr, nullptr};   // ... and have been copied to the host
   cudaEvent_t entry = nullptr;
   cudaEvent_t copy_done = nullptr;
   uint32_t* err = nullptr;  // 256-byte status word allocation
@@ -81,6 +85,10 @@ int dev_state(int dev, DevState** out) {
       UPIPE_CUDA(cudaEventCreateWithFlags(&d.slot_free[i], cudaEventDisableTiming));
       UPIPE_CUDA(cudaEventCreateWithFlags(&d.dkdv_done[i], cudaEventDisableTiming));
       UPIPE_CUDA(cudaEventCreateWithFlags(&d.dkdv_free[i], cudaEventDisableTiming));
+      UPIPE_CUDA(cudaEventCreateWithFlags(&d.act_ready[i], cudaEventDisableTiming));
+      UPIPE_CUDA(cudaEventCreateWithFlags(&d.act_free[i], cudaEventDisableTiming));
+      UPIPE_CUDA(cudaEventCreateWithFlags(&d.out_done[i], cudaEventDisableTiming));
+      UPIPE_CUDA(cudaEventCreateWithFlags(&d.out_free[i], cudaEventDisableTiming));
     }
     UPIPE_CUDA(cudaEventCreateWithFlags(&d.entry, cudaEventDisableTiming));
     UPIPE_CUDA(cudaEventCreateWithFlags(&d.copy_done, cudaEventDisableTiming));
@@ -180,18 +188,22 @@ struct Plan {
   int64_t S = 0, T = 0, S_pad = 0, T_pad = 0;
   int n_trunks = 0;
   bool kv_host = false;
+  bool act_host = false;  // q/o (and dout/dq) may be pinned host memory: staging reserved
   // forward segments
   size_t f_qw = 0, f_kw = 0, f_vw = 0, f_slot_k[2] = {0, 0}, f_slot_v[2] = {0, 0};
+  size_t f_qw2 = 0, f_ostg[2] = {0, 0};  // host activations: second Q buffer, O staging
   size_t f_state_o = 0, f_state_ml = 0, f_total = 0;
   // backward segments
   size_t b_qw = 0, b_dow = 0, b_kw = 0, b_vw = 0, b_slot_k[2] = {0, 0}, b_slot_v[2] = {0, 0};
   size_t b_slot_dk[2] = {0, 0}, b_slot_dv[2] = {0, 0};  // host-K/V mode: dK/dV trunk slots
+  // host activations: second Q and dO buffers, head-major O copies, dQ output stagings
+  size_t b_qw2 = 0, b_dow2 = 0, b_ow[2] = {0, 0}, b_dqs[2] = {0, 0};
   size_t b_dqacc = 0, b_lse2 = 0, b_dvec = 0, b_total = 0;
 };
 
 // Validates shapes (no device access). Returns UPIPE_OK and fills the plan.
 int make_plan(int B, int64_t S, int Hq, int Hkv, int D, int causal, int head_chunk,
-              int64_t seq_trunk, int kv_on_host, Plan* p) {
+              int64_t seq_trunk, int host_mask, Plan* p) {
   if (B < 1 || S < 1 || Hq < 1 || Hkv < 1 || D < 1)
     return fail(UPIPE_ERR_INVALID_ARG, "sizes must be positive (B=%d S=%lld Hq=%d Hkv=%d D=%d)",
                 B, static_cast<long long>(S), Hq, Hkv, D);
@@ -216,7 +228,8 @@ int make_plan(int B, int64_t S, int Hq, int Hkv, int D, int causal, int head_chu
   p->S_pad = (S + 127) / 128 * 128;
   p->T_pad = (T + 127) / 128 * 128;
   p->n_trunks = static_cast<int>((S + T - 1) / T);
-  p->kv_host = kv_on_host != 0;
+  p->kv_host = (host_mask & UPIPE_HOST_KV) != 0;
+  p->act_host = (host_mask & UPIPE_HOST_ACT) != 0;
 
   const size_t hcB = static_cast<size_t>(B) * p->hc, kcB = static_cast<size_t>(B) * p->kc;
   const size_t qw = hcB * S * D * 2, kvw = kcB * S * D * 2, slot = kcB * T * D * 2;
@@ -228,6 +241,12 @@ int make_plan(int B, int64_t S, int Hq, int Hkv, int D, int causal, int head_chu
   };
   // forward
   p->f_qw = take(qw);
+  if (p->act_host) {
+    // host q: a second head-major Q buffer so the next group's Q is staged during this one;
+    // host o: two [B, S, hc, D] staging buffers, copied out while the next group computes
+    p->f_qw2 = take(qw);
+    for (int i = 0; i < 2; ++i) p->f_ostg[i] = take(qw);
+  }
   if (p->kv_host) {
     for (int i = 0; i < 2; ++i) { p->f_slot_k[i] = take(slot); p->f_slot_v[i] = take(slot); }
   } else {
@@ -254,6 +273,12 @@ int make_plan(int B, int64_t S, int Hq, int Hkv, int D, int causal, int head_chu
   } else {
     p->b_kw = take(kvw);
     p->b_vw = take(kvw);
+  }
+  if (p->act_host) {
+    p->b_qw2 = take(qw);
+    p->b_dow2 = take(qw);
+    for (int i = 0; i < 2; ++i) p->b_ow[i] = take(qw);
+    for (int i = 0; i < 2; ++i) p->b_dqs[i] = take(qw);
   }
   p->b_dqacc = take(hcB * p->S_pad * D * 4);
   p->b_lse2 = take(hcB * p->S_pad * 4);
@@ -333,6 +358,36 @@ int unstage_trunk(const Plan& p, const uint8_t* slot, void* dst, int kvh0, int64
   return UPIPE_OK;
 }
 
+// Host -> device copy of heads [h0, h0+hc) of a token-major [B,S,H,D] tensor into a head-major
+// [B*hc][S][D] buffer: one 2-D copy (rows of D elements) per (batch row, head).
+int stage_heads(const void* src, void* dst, int B, int64_t S, int H, int D, int h0, int hc,
+                cudaStream_t copy) {
+  const size_t row = static_cast<size_t>(D) * 2;
+  for (int b = 0; b < B; ++b)
+    for (int c = 0; c < hc; ++c) {
+      const uint8_t* s = static_cast<const uint8_t*>(src) +
+                         (static_cast<size_t>(b) * S * H + h0 + c) * row;
+      uint8_t* d = static_cast<uint8_t*>(dst) + (static_cast<size_t>(b) * hc + c) * S * row;
+      UPIPE_CUDA(cudaMemcpy2DAsync(d, row, s, static_cast<size_t>(H) * row, row,
+                                   static_cast<size_t>(S), cudaMemcpyHostToDevice, copy));
+    }
+  return UPIPE_OK;
+}
+
+// Device -> host copy of a group staging [B,S,hc,D] into heads [h0, h0+hc) of a token-major
+// [B,S,H,D] tensor: one 2-D copy per batch row.
+int unstage_heads(const void* stg, void* dst, int B, int64_t S, int H, int D, int h0, int hc,
+                  cudaStream_t copy) {
+  const size_t row = static_cast<size_t>(D) * 2, w = row * hc;
+  for (int b = 0; b < B; ++b) {
+    uint8_t* d = static_cast<uint8_t*>(dst) + (static_cast<size_t>(b) * S * H + h0) * row;
+    const uint8_t* s = static_cast<const uint8_t*>(stg) + static_cast<size_t>(b) * S * w;
+    UPIPE_CUDA(cudaMemcpy2DAsync(d, static_cast<size_t>(H) * row, s, w, w,
+                                 static_cast<size_t>(S), cudaMemcpyDeviceToHost, copy));
+  }
+  return UPIPE_OK;
+}
+
 // Double-buffered trunk stager shared by forward and backward.
 struct Stager {
   const Plan& p;
@@ -384,9 +439,9 @@ using namespace upipe;
 extern "C" {
 
 size_t upipe_workspace_bytes(int B, int64_t S, int Hq, int Hkv, int D, int causal,
-                             int head_chunk, int64_t seq_trunk, int pass, int kv_on_host) {
+                             int head_chunk, int64_t seq_trunk, int pass, int host_mask) {
   Plan p;
-  if (make_plan(B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk, kv_on_host, &p) != UPIPE_OK)
+  if (make_plan(B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk, host_mask, &p) != UPIPE_OK)
     return 0;
   if (pass == UPIPE_PASS_FWD) return p.f_total;
   if (pass == UPIPE_PASS_BWD) return p.b_total;
@@ -408,14 +463,29 @@ int upipe_attn_fwd(const void* q, const void* k, const void* v, void* o, float* 
   Plan p0;
   int st = make_plan(B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk, 0, &p0);
   if (st != UPIPE_OK) return st;
-  const void* dptrs[4] = {q, o, workspace, lse};
-  const char* names[4] = {"q", "o", "workspace", "lse"};
+  // q and o: device memory of the call's device, or pinned host memory (each on its own)
+  int dq_dev = -1, do_dev = -1;
+  const int kq = pointer_kind(q, &dq_dev), ko = pointer_kind(o, &do_dev);
+  if (kq < 0 || ko < 0)
+    return fail(UPIPE_ERR_INVALID_ARG, "q and o must be device memory or pinned host memory");
+  const bool q_host = kq == 1, o_host = ko == 1;
+  const void* dptrs[4] = {workspace, lse, q, o};
+  const char* names[4] = {"workspace", "lse", "q", "o"};
+  const void* dlist[4];
+  const char* nlist[4];
+  int nd = 0;
+  for (int i = 0; i < 4; ++i) {
+    if (!dptrs[i] || (i == 2 && q_host) || (i == 3 && o_host)) continue;
+    dlist[nd] = dptrs[i];
+    nlist[nd++] = names[i];
+  }
   bool kv_host = false;
   int dev = 0;
-  st = check_placement(dptrs, lse ? 4 : 3, names, k, v, &kv_host, &dev);
+  st = check_placement(dlist, nd, nlist, k, v, &kv_host, &dev);
   if (st != UPIPE_OK) return st;
   Plan p;
-  make_plan(B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk, kv_host ? 1 : 0, &p);
+  make_plan(B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk,
+            (kv_host ? UPIPE_HOST_KV : 0) | (q_host || o_host ? UPIPE_HOST_ACT : 0), &p);
   if (workspace_bytes < p.f_total)
     return fail(UPIPE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes,
                 p.f_total);
@@ -427,7 +497,6 @@ int upipe_attn_fwd(const void* q, const void* k, const void* v, void* o, float* 
   if (st != UPIPE_OK) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  void* qw = ws + p.f_qw;
   float* state_o = p.n_trunks > 1 ? reinterpret_cast<float*>(ws + p.f_state_o) : nullptr;
   float* state_ml = p.n_trunks > 1 ? reinterpret_cast<float*>(ws + p.f_state_ml) : nullptr;
   const float scale = 1.0f / std::sqrt(static_cast<float>(D));
@@ -438,10 +507,29 @@ int upipe_attn_fwd(const void* q, const void* k, const void* v, void* o, float* 
     // one staging job per (group, key/value trunk): the trunk serves every query trunk
     for (int g = 0; g < Hq / p.hc; ++g)
       for (int n = 0; n < p.n_trunks; ++n) stg.jobs.push_back({g * p.kc, n});
+  }
+  if (kv_host || q_host || o_host) {
     // The copy stream must not touch the workspace before earlier work on `stream` is done.
     UPIPE_CUDA(cudaEventRecord(ds->entry, stream));
     UPIPE_CUDA(cudaStreamWaitEvent(ds->copy, ds->entry, 0));
   }
+  const int n_groups = Hq / p.hc;
+  auto q_buf = [&](int g) -> uint8_t* { return ws + ((q_host && (g & 1)) ? p.f_qw2 : p.f_qw); };
+  // host q: group g's heads go into Q buffer g%2 once group g-2 no longer reads it
+  auto stage_q = [&](int g) -> int {
+    const int s = g & 1;
+    if (g >= 2) UPIPE_CUDA(cudaStreamWaitEvent(ds->copy, ds->act_free[s], 0));
+    const int r = stage_heads(q, q_buf(g), B, S, Hq, D, g * p.hc, p.hc, ds->copy);
+    if (r != UPIPE_OK) return r;
+    UPIPE_CUDA(cudaEventRecord(ds->act_ready[s], ds->copy));
+    return UPIPE_OK;
+  };
+  if (q_host) {
+    st = stage_q(0);
+    if (st != UPIPE_OK) return st;
+  }
+  // host o: group g's kernels write a [B, S, hc, D] staging buffer, copied out afterwards
+  void* o_out = o;
   auto launch = [&](const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, int h0,
                     int m, int n, int64_t row_lo, int64_t row_hi, int64_t pos0,
                     int64_t state_stride) -> int {
@@ -453,7 +541,8 @@ int upipe_attn_fwd(const void* q, const void* k, const void* v, void* o, float* 
     a.hc = p.hc; a.kc = p.kc; a.G = p.G; a.Hq = Hq; a.h0 = h0;
     a.causal = causal; a.first = (n == 0); a.last = (n == n_last);
     a.scale_log2 = scale * 1.4426950408889634f;
-    a.o = o; a.lse = lse;
+    a.o = o_out; a.lse = lse;
+    if (o_host) { a.o_heads = p.hc; a.o_head0 = 0; }
     // with an S-sized state the rows of query trunk m start m*T rows in
     const int64_t soff = state_stride ? a.q_lo : 0;
     a.state_o = state_o ? state_o + soff * D : nullptr;
@@ -467,15 +556,30 @@ int upipe_attn_fwd(const void* q, const void* k, const void* v, void* o, float* 
     return UPIPE_OK;
   };
   int job = 0;
-  for (int g = 0; g < Hq / p.hc; ++g) {
+  for (int g = 0; g < n_groups; ++g) {
     const int h0 = g * p.hc, kvh0 = g * p.kc;
-    UPIPE_CUDA(launch_seq_to_head(q, qw, B, S, Hq, D, h0, p.hc, stream));
+    const int gs = g & 1;
+    uint8_t* qwg = q_buf(g);
+    if (q_host) {
+      if (g + 1 < n_groups) {  // prefetch the next group's Q while this group computes
+        st = stage_q(g + 1);
+        if (st != UPIPE_OK) return st;
+      }
+      UPIPE_CUDA(cudaStreamWaitEvent(stream, ds->act_ready[gs], 0));
+    } else {
+      UPIPE_CUDA(launch_seq_to_head(q, qwg, B, S, Hq, D, h0, p.hc, stream));
+    }
+    if (o_host) {
+      // the staging this group writes must have reached the host from group g-2
+      if (g >= 2) UPIPE_CUDA(cudaStreamWaitEvent(stream, ds->out_free[gs], 0));
+      o_out = ws + p.f_ostg[gs];
+    }
     if (!kv_host) {
       UPIPE_CUDA(launch_seq_to_head(k, ws + p.f_kw, B, S, Hkv, D, kvh0, p.kc, stream));
       UPIPE_CUDA(launch_seq_to_head(v, ws + p.f_vw, B, S, Hkv, D, kvh0, p.kc, stream));
     }
     CUtensorMap tq, tk, tv;
-    UPIPE_CUDA(make_tmap_bf16(&tq, qw, D, S, static_cast<int64_t>(B) * p.hc));
+    UPIPE_CUDA(make_tmap_bf16(&tq, qwg, D, S, static_cast<int64_t>(B) * p.hc));
     if (!kv_host) {
       // FPDT order: query trunk m folds key/value trunks 0..m into a T-row state
       UPIPE_CUDA(make_tmap_bf16(&tk, ws + p.f_kw, D, S, static_cast<int64_t>(B) * p.kc));
@@ -488,25 +592,40 @@ int upipe_attn_fwd(const void* q, const void* k, const void* v, void* o, float* 
           if (st != UPIPE_OK) return st;
         }
       }
-      continue;
-    }
-    // Host K/V: key/value trunk n is staged once and then met by every query trunk that sees
-    // it (m >= n when causal); each query trunk keeps its running state in an S-sized buffer.
-    for (int n = 0; n < p.n_trunks; ++n, ++job) {
-      const int64_t t0 = static_cast<int64_t>(n) * p.T;
-      const int64_t Tn = std::min<int64_t>(p.T, S - t0);
-      st = stg.before(job);
-      if (st != UPIPE_OK) return st;
-      const int s = job & 1;
-      UPIPE_CUDA(make_tmap_bf16(&tk, stg.slot_k[s], D, Tn, static_cast<int64_t>(B) * p.kc));
-      UPIPE_CUDA(make_tmap_bf16(&tv, stg.slot_v[s], D, Tn, static_cast<int64_t>(B) * p.kc));
-      for (int m = causal ? n : 0; m < p.n_trunks; ++m) {
-        st = launch(tq, tk, tv, h0, m, n, 0, Tn, t0, p.n_trunks > 1 ? p.S_pad : 0);
+    } else {
+      // Host K/V: key/value trunk n is staged once and then met by every query trunk that
+      // sees it (m >= n when causal); each query trunk keeps its running state in an S-sized
+      // buffer.
+      for (int n = 0; n < p.n_trunks; ++n, ++job) {
+        const int64_t t0 = static_cast<int64_t>(n) * p.T;
+        const int64_t Tn = std::min<int64_t>(p.T, S - t0);
+        st = stg.before(job);
+        if (st != UPIPE_OK) return st;
+        const int s = job & 1;
+        UPIPE_CUDA(make_tmap_bf16(&tk, stg.slot_k[s], D, Tn, static_cast<int64_t>(B) * p.kc));
+        UPIPE_CUDA(make_tmap_bf16(&tv, stg.slot_v[s], D, Tn, static_cast<int64_t>(B) * p.kc));
+        for (int m = causal ? n : 0; m < p.n_trunks; ++m) {
+          st = launch(tq, tk, tv, h0, m, n, 0, Tn, t0, p.n_trunks > 1 ? p.S_pad : 0);
+          if (st != UPIPE_OK) return st;
+        }
+        st = stg.after(job);
         if (st != UPIPE_OK) return st;
       }
-      st = stg.after(job);
-      if (st != UPIPE_OK) return st;
     }
+    // end of group g: its Q buffer is free again; its O staging goes to the host
+    if (q_host) UPIPE_CUDA(cudaEventRecord(ds->act_free[gs], stream));
+    if (o_host) {
+      UPIPE_CUDA(cudaEventRecord(ds->out_done[gs], stream));
+      UPIPE_CUDA(cudaStreamWaitEvent(ds->copy, ds->out_done[gs], 0));
+      st = unstage_heads(ws + p.f_ostg[gs], o, B, S, Hq, D, h0, p.hc, ds->copy);
+      if (st != UPIPE_OK) return st;
+      UPIPE_CUDA(cudaEventRecord(ds->out_free[gs], ds->copy));
+    }
+  }
+  if (o_host) {
+    // the caller's stream completes only after the last group's O reached the host
+    UPIPE_CUDA(cudaEventRecord(ds->copy_done, ds->copy));
+    UPIPE_CUDA(cudaStreamWaitEvent(stream, ds->copy_done, 0));
   }
   return UPIPE_OK;
 }
@@ -526,11 +645,33 @@ int upipe_attn_bwd(const void* q, const void* k, const void* v, const void* o, c
   Plan p0;
   int st = make_plan(B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk, 0, &p0);
   if (st != UPIPE_OK) return st;
-  const void* dptrs[6] = {q, o, lse, dout, dq, workspace};
-  const char* names[6] = {"q", "o", "lse", "dout", "dq", "workspace"};
+  // q, o, dout, dq: device memory of the call's device, or pinned host memory (each on its own)
+  const void* act[4] = {q, o, dout, dq};
+  const char* act_names[4] = {"q", "o", "dout", "dq"};
+  bool act_host[4];
+  const void* dlist[6] = {lse, workspace};
+  const char* nlist[6] = {"lse", "workspace"};
+  int nd = 2;
+  for (int i = 0; i < 4; ++i) {
+    int d = -1;
+    const int kind = pointer_kind(act[i], &d);
+    if (kind < 0)
+      return fail(UPIPE_ERR_INVALID_ARG, "%s must be device memory or pinned host memory",
+                  act_names[i]);
+    act_host[i] = kind == 1;
+    if (!act_host[i]) {
+      dlist[nd] = act[i];
+      nlist[nd++] = act_names[i];
+    }
+  }
+  const bool q_host = act_host[0], o_host = act_host[1], dout_host = act_host[2],
+             dq_host = act_host[3];
+  const bool any_act = q_host || o_host || dout_host || dq_host;
+  // with a host o or dout the pre-pass reads head-major copies of both
+  const bool hm_pre = o_host || dout_host;
   bool kv_host = false;
   int dev = 0;
-  st = check_placement(dptrs, 6, names, k, v, &kv_host, &dev);
+  st = check_placement(dlist, nd, nlist, k, v, &kv_host, &dev);
   if (st != UPIPE_OK) return st;
   // dk/dv: device memory, or (with host k/v) both pinned host memory, written trunk by trunk
   int ddk = -1, ddv = -1;
@@ -543,7 +684,8 @@ int upipe_attn_bwd(const void* q, const void* k, const void* v, const void* o, c
   if (dkdv_host && !kv_host)
     return fail(UPIPE_ERR_INVALID_ARG, "dk/dv may be pinned host memory only when k/v are too");
   Plan p;
-  make_plan(B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk, kv_host ? 1 : 0, &p);
+  make_plan(B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk,
+            (kv_host ? UPIPE_HOST_KV : 0) | (any_act ? UPIPE_HOST_ACT : 0), &p);
   if (workspace_bytes < p.b_total)
     return fail(UPIPE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes,
                 p.b_total);
@@ -555,8 +697,6 @@ int upipe_attn_bwd(const void* q, const void* k, const void* v, const void* o, c
   if (st != UPIPE_OK) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  void* qw = ws + p.b_qw;
-  void* dow = ws + p.b_dow;
   float* dqacc = reinterpret_cast<float*>(ws + p.b_dqacc);
   float* lse2 = reinterpret_cast<float*>(ws + p.b_lse2);
   float* dvec = reinterpret_cast<float*>(ws + p.b_dvec);
@@ -567,15 +707,61 @@ int upipe_attn_bwd(const void* q, const void* k, const void* v, const void* o, c
   if (kv_host) {
     for (int g = 0; g < Hq / p.hc; ++g)
       for (int n = 0; n < p.n_trunks; ++n) stg.jobs.push_back({g * p.kc, n});
+  }
+  if (kv_host || any_act) {
+    // The copy stream must not touch the workspace before earlier work on `stream` is done.
     UPIPE_CUDA(cudaEventRecord(ds->entry, stream));
     UPIPE_CUDA(cudaStreamWaitEvent(ds->copy, ds->entry, 0));
   }
+  const int n_groups = Hq / p.hc;
+  // Per head group g, buffers g%2 when host activations rotate through them.
+  auto qw_of = [&](int g) -> uint8_t* { return ws + ((q_host && (g & 1)) ? p.b_qw2 : p.b_qw); };
+  auto dow_of = [&](int g) -> uint8_t* {
+    return ws + ((hm_pre && (g & 1)) ? p.b_dow2 : p.b_dow);
+  };
+  auto ow_of = [&](int g) -> uint8_t* { return ws + p.b_ow[g & 1]; };
+  const bool stage_any = q_host || o_host || dout_host;
+  // host q / o / dout: group g's heads are copied head-major once group g-2 is done with them
+  auto stage_act = [&](int g) -> int {
+    const int s = g & 1, h0 = g * p.hc;
+    if (g >= 2) UPIPE_CUDA(cudaStreamWaitEvent(ds->copy, ds->act_free[s], 0));
+    int r = UPIPE_OK;
+    if (q_host) r = stage_heads(q, qw_of(g), B, S, Hq, D, h0, p.hc, ds->copy);
+    if (r == UPIPE_OK && o_host) r = stage_heads(o, ow_of(g), B, S, Hq, D, h0, p.hc, ds->copy);
+    if (r == UPIPE_OK && dout_host)
+      r = stage_heads(dout, dow_of(g), B, S, Hq, D, h0, p.hc, ds->copy);
+    if (r != UPIPE_OK) return r;
+    UPIPE_CUDA(cudaEventRecord(ds->act_ready[s], ds->copy));
+    return UPIPE_OK;
+  };
+  if (stage_any) {
+    st = stage_act(0);
+    if (st != UPIPE_OK) return st;
+  }
   int job = 0;
-  for (int g = 0; g < Hq / p.hc; ++g) {
+  for (int g = 0; g < n_groups; ++g) {
     const int h0 = g * p.hc, kvh0 = g * p.kc;
-    UPIPE_CUDA(launch_seq_to_head(q, qw, B, S, Hq, D, h0, p.hc, stream));
-    UPIPE_CUDA(launch_bwd_pre(o, dout, lse, dow, dvec, lse2, dqacc, B, S, p.S_pad, Hq, D, h0,
-                              p.hc, scale, stream));
+    const int gs = g & 1;
+    void* qw = qw_of(g);
+    void* dow = dow_of(g);
+    if (stage_any) {
+      if (g + 1 < n_groups) {  // prefetch the next group's activations
+        st = stage_act(g + 1);
+        if (st != UPIPE_OK) return st;
+      }
+      UPIPE_CUDA(cudaStreamWaitEvent(stream, ds->act_ready[gs], 0));
+    }
+    if (!q_host) UPIPE_CUDA(launch_seq_to_head(q, qw, B, S, Hq, D, h0, p.hc, stream));
+    if (hm_pre) {
+      void* ow = ow_of(g);
+      if (!o_host) UPIPE_CUDA(launch_seq_to_head(o, ow, B, S, Hq, D, h0, p.hc, stream));
+      if (!dout_host) UPIPE_CUDA(launch_seq_to_head(dout, dow, B, S, Hq, D, h0, p.hc, stream));
+      UPIPE_CUDA(launch_bwd_pre(ow, dow, lse, dow, dvec, lse2, dqacc, B, S, p.S_pad, Hq, D, h0,
+                                p.hc, scale, 1, stream));
+    } else {
+      UPIPE_CUDA(launch_bwd_pre(o, dout, lse, dow, dvec, lse2, dqacc, B, S, p.S_pad, Hq, D, h0,
+                                p.hc, scale, 0, stream));
+    }
     if (!kv_host) {
       UPIPE_CUDA(launch_seq_to_head(k, ws + p.b_kw, B, S, Hkv, D, kvh0, p.kc, stream));
       UPIPE_CUDA(launch_seq_to_head(v, ws + p.b_vw, B, S, Hkv, D, kvh0, p.kc, stream));
@@ -630,10 +816,23 @@ int upipe_attn_bwd(const void* q, const void* k, const void* v, const void* o, c
         UPIPE_CUDA(cudaEventRecord(ds->dkdv_free[s], ds->copy));
       }
     }
-    UPIPE_CUDA(launch_dq_convert(dqacc, dq, B, S, p.S_pad, Hq, D, h0, p.hc, stream));
+    if (stage_any) UPIPE_CUDA(cudaEventRecord(ds->act_free[gs], stream));
+    if (dq_host) {
+      // this group's dQ goes to staging g%2 (free once group g-2's copy-out is done), then out
+      if (g >= 2) UPIPE_CUDA(cudaStreamWaitEvent(stream, ds->out_free[gs], 0));
+      UPIPE_CUDA(launch_dq_convert(dqacc, ws + p.b_dqs[gs], B, S, p.S_pad, p.hc, D, 0, p.hc,
+                                   stream));
+      UPIPE_CUDA(cudaEventRecord(ds->out_done[gs], stream));
+      UPIPE_CUDA(cudaStreamWaitEvent(ds->copy, ds->out_done[gs], 0));
+      st = unstage_heads(ws + p.b_dqs[gs], dq, B, S, Hq, D, h0, p.hc, ds->copy);
+      if (st != UPIPE_OK) return st;
+      UPIPE_CUDA(cudaEventRecord(ds->out_free[gs], ds->copy));
+    } else {
+      UPIPE_CUDA(launch_dq_convert(dqacc, dq, B, S, p.S_pad, Hq, D, h0, p.hc, stream));
+    }
   }
-  if (dkdv_host) {
-    // the caller's stream completes only after the last dK/dV trunk reached the host
+  if (dkdv_host || dq_host) {
+    // the caller's stream completes only after the last copy to the host
     UPIPE_CUDA(cudaEventRecord(ds->copy_done, ds->copy));
     UPIPE_CUDA(cudaStreamWaitEvent(stream, ds->copy_done, 0));
   }
@@ -721,6 +920,10 @@ void upipe_shutdown(void) {
       cudaEventDestroy(d.slot_free[s]);
       cudaEventDestroy(d.dkdv_done[s]);
       cudaEventDestroy(d.dkdv_free[s]);
+      cudaEventDestroy(d.act_ready[s]);
+      cudaEventDestroy(d.act_free[s]);
+      cudaEventDestroy(d.out_done[s]);
+      cudaEventDestroy(d.out_free[s]);
     }
     cudaEventDestroy(d.entry);
     cudaEventDestroy(d.copy_done);

@@ -323,7 +323,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (a.last) {
         const float inv_l = 1.f / l_sum;
         __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.o) +
-                              ((static_cast<int64_t>(b) * a.S + qrow) * a.Hq + a.h0 + hl) * D;
+                              ((static_cast<int64_t>(b) * a.S + qrow) * (a.o_heads ? a.o_heads : a.Hq) +
+                               (a.o_heads ? a.o_head0 : a.h0) + hl) * D;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];

@@ -33,7 +33,8 @@ struct FwdArgs {
   int hc, kc, G, Hq, h0;         // group q-heads, group kv-heads, Hq/Hkv, total q-heads, first q-head
   int causal, first, last;       // first: no carried state; last: finalise O and LSE
   float scale_log2;              // softmax scale * log2(e)
-  void* o;                       // [B,S,Hq,D] bf16, written when last
+  void* o;                       // bf16, written when last: [B,S,Hq,D], or a staging [B,S,o_heads,D]
+  int o_heads, o_head0;          // heads per row of o and this group's first; 0 means Hq and h0
   float* lse;                    // [B,Hq,S], written when last
   float* state_o;                // [B*hc][state_stride][D] fp32 running numerator (rows from q_lo)
   float* state_ml;               // [B*hc][state_stride][2] fp32 running max (log2 units), sum
@@ -95,14 +96,18 @@ cudaError_t launch_head_to_seq(const void* src, void* dst, int B, int64_t S, int
 //   (stored negated: the kernels add them with one fused multiply-add)
 //   dqacc[(b*hc+h)*S_pad + s][:] = 0
 // rows s in [S, S_pad) get dvec = lse2 = 0 and zeroed dqacc.
+// head_major_in: o and dout are this group's head-major [B*hc][S][D] copies (dout == dow,
+// not rewritten) instead of the token-major tensors.
 cudaError_t launch_bwd_pre(const void* o, const void* dout, const float* lse, void* dow,
                            float* dvec, float* lse2, float* dqacc, int B, int64_t S,
                            int64_t S_pad, int Hq, int D, int h0, int hc, float scale,
-                           cudaStream_t stream);
+                           int head_major_in, cudaStream_t stream);
 
 // dq[b][s][h0+h][:] = bf16(dqacc[(b*hc+h)*S_pad + s][:])
+// dq rows of out_heads heads, this group's at [out_head0, out_head0 + hc): (Hq, h0) for the
+// token-major output, (hc, 0) for a group staging [B,S,hc,D].
 cudaError_t launch_dq_convert(const float* dqacc, void* dq, int B, int64_t S, int64_t S_pad,
-                              int Hq, int D, int h0, int hc, cudaStream_t stream);
+                              int out_heads, int D, int out_head0, int hc, cudaStream_t stream);
 
 // ---- self-tests (selftest.cu) --------------------------------------------------------------
 cudaError_t launch_selftest_umma(const void* a, const void* b, float* c, int N, int K,

@@ -65,12 +65,14 @@ __global__ void head_to_seq_kernel(const uint4* __restrict__ src, uint4* __restr
 }
 
 // One group of Dc = D/8 consecutive lanes handles one (b, s, h) row; Dc is 8 or 16 and
-// divides the warp, so the row reduction stays inside a warp.
+// divides the warp, so the row reduction stays inside a warp. o and dout are token-major
+// [B,S,Hq,D] (dout is gathered into dow on the way), or, with head_major_in, this group's
+// head-major [B*hc][S][D] copies (dout then already is dow, which is not written).
 __global__ void bwd_pre_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout,
                                const float* __restrict__ lse, uint4* __restrict__ dow,
                                float* __restrict__ dvec, float* __restrict__ lse2,
                                float4* __restrict__ dqacc, int B, int64_t S, int64_t S_pad, int Hq,
-                               int Dc, int h0, int hc, float scale) {
+                               int Dc, int h0, int hc, float scale, int head_major_in) {
   const int64_t rows = static_cast<int64_t>(B) * S_pad * hc;
   const int64_t total = rows * Dc;
   const float kLog2e = 1.4426950408889634f;
@@ -88,10 +90,11 @@ __global__ void bwd_pre_kernel(const uint4* __restrict__ o, const uint4* __restr
     const int64_t zrow = (b * hc + h) * S_pad + s;  // row of dvec / lse2 / dqacc
     if (live) {
       if (s < S) {
-        const int64_t tok = ((b * S + s) * Hq + h0 + h) * Dc + c;
+        const int64_t hm = ((b * hc + h) * S + s) * Dc + c;
+        const int64_t tok = head_major_in ? hm : ((b * S + s) * Hq + h0 + h) * Dc + c;
         const uint4 ov = __ldg(o + tok);
         const uint4 dv = __ldg(dout + tok);
-        dow[((b * hc + h) * S + s) * Dc + c] = dv;
+        if (!head_major_in) dow[hm] = dv;
         const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
         const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
 #pragma unroll
@@ -114,8 +117,11 @@ __global__ void bwd_pre_kernel(const uint4* __restrict__ o, const uint4* __restr
   }
 }
 
+// dq rows hold out_heads heads; this group's go to heads [out_head0, out_head0 + hc): the
+// token-major [B,S,Hq,D] output (Hq, h0) or a group staging [B,S,hc,D] (hc, 0).
 __global__ void dq_convert_kernel(const float4* __restrict__ dqacc, uint4* __restrict__ dq, int B,
-                                  int64_t S, int64_t S_pad, int Hq, int Dc, int h0, int hc) {
+                                  int64_t S, int64_t S_pad, int out_heads, int Dc, int out_head0,
+                                  int hc) {
   const int64_t total = static_cast<int64_t>(B) * S * hc * Dc;
   for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
        idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -130,7 +136,7 @@ __global__ void dq_convert_kernel(const float4* __restrict__ dqacc, uint4* __res
     const float4 y = dqacc[zrow * 2 * Dc + 2 * c + 1];
     __nv_bfloat162 w[4] = {__floats2bfloat162_rn(x.x, x.y), __floats2bfloat162_rn(x.z, x.w),
                            __floats2bfloat162_rn(y.x, y.y), __floats2bfloat162_rn(y.z, y.w)};
-    dq[((b * S + s) * Hq + h0 + h) * Dc + c] = *reinterpret_cast<const uint4*>(w);
+    dq[((b * S + s) * out_heads + out_head0 + h) * Dc + c] = *reinterpret_cast<const uint4*>(w);
   }
 }
 
@@ -163,27 +169,27 @@ cudaError_t launch_head_to_seq(const void* src, void* dst, int B, int64_t S, int
 cudaError_t launch_bwd_pre(const void* o, const void* dout, const float* lse, void* dow,
                            float* dvec, float* lse2, float* dqacc, int B, int64_t S,
                            int64_t S_pad, int Hq, int D, int h0, int hc, float scale,
-                           cudaStream_t stream) {
+                           int head_major_in, cudaStream_t stream) {
   const int Dc = D / 8;
   const int64_t work = static_cast<int64_t>(B) * S_pad * hc * Dc;
   launch_begin(2, stream);
   bwd_pre_kernel<<<grid_for(work, kLayoutThreads), kLayoutThreads, 0, stream>>>(
       static_cast<const uint4*>(o), static_cast<const uint4*>(dout), lse,
       static_cast<uint4*>(dow), dvec, lse2, reinterpret_cast<float4*>(dqacc), B, S, S_pad, Hq, Dc,
-      h0, hc, scale);
+      h0, hc, scale, head_major_in);
   cudaError_t e = cudaGetLastError();
   launch_end(2, stream);
   return e;
 }
 
 cudaError_t launch_dq_convert(const float* dqacc, void* dq, int B, int64_t S, int64_t S_pad,
-                              int Hq, int D, int h0, int hc, cudaStream_t stream) {
+                              int out_heads, int D, int out_head0, int hc, cudaStream_t stream) {
   const int Dc = D / 8;
   const int64_t work = static_cast<int64_t>(B) * S * hc * Dc;
   launch_begin(4, stream);
   dq_convert_kernel<<<grid_for(work, kLayoutThreads), kLayoutThreads, 0, stream>>>(
-      reinterpret_cast<const float4*>(dqacc), static_cast<uint4*>(dq), B, S, S_pad, Hq, Dc, h0,
-      hc);
+      reinterpret_cast<const float4*>(dqacc), static_cast<uint4*>(dq), B, S, S_pad, out_heads, Dc,
+      out_head0, hc);
   cudaError_t e = cudaGetLastError();
   launch_end(4, stream);
   return e;

@@ -60,6 +60,11 @@ typedef enum {
 /* Which pass a workspace is sized for. */
 enum { UPIPE_PASS_FWD = 0, UPIPE_PASS_BWD = 1, UPIPE_PASS_BOTH = 2 };
 
+/* What may live in pinned host memory (bits of upipe_workspace_bytes' host_mask):
+ * UPIPE_HOST_KV: k and v (and then dk, dv); UPIPE_HOST_ACT: q and o in the forward, q, o, dout
+ * and dq in the backward (each independently of the others). */
+enum { UPIPE_HOST_KV = 1, UPIPE_HOST_ACT = 2 };
+
 /*
  * Bytes of device workspace one upipe_attn_fwd / upipe_attn_bwd call needs.
  * Pure host arithmetic; touches no device. Returns 0 for arguments that the matching
@@ -68,28 +73,36 @@ enum { UPIPE_PASS_FWD = 0, UPIPE_PASS_BWD = 1, UPIPE_PASS_BOTH = 2 };
  * unchunked one at the same seq_trunk - the activation-memory cut UPipe reports (UPipe
  * abstract, arXiv 2602.21196: up to 87.5% for a 32B model, i.e. 8 of 64 heads).
  *   pass: UPIPE_PASS_FWD, UPIPE_PASS_BWD or UPIPE_PASS_BOTH (the max of the two).
- *   kv_on_host: 1 if k/v will be pinned host memory (two trunk slots instead of full K/V;
- *     the forward then walks key/value trunks outermost, staging each once, and keeps every
- *     query trunk's fp32 running state: head_chunk*S*(D+2)*4 bytes per batch row; the
- *     backward also reserves two dK and two dV trunk slots, used when dk/dv are pinned host
- *     memory as well).
+ *   host_mask: UPIPE_HOST_KV if k/v will be pinned host memory (two trunk slots instead of
+ *     full K/V; the forward then walks key/value trunks outermost, staging each once, and
+ *     keeps every query trunk's fp32 running state: head_chunk*S*(D+2)*4 bytes per batch
+ *     row; the backward also reserves two dK and two dV trunk slots, used when dk/dv are
+ *     pinned host memory as well). | UPIPE_HOST_ACT if any of q, o, dout, dq will be pinned
+ *     host memory (per pass, a few head-group-sized staging buffers so that each group's
+ *     activations move in and out while the neighbouring group computes). 1 keeps meaning
+ *     host k/v, as in earlier versions of this interface.
  */
 size_t upipe_workspace_bytes(int B, int64_t S, int Hq, int Hkv, int D, int causal,
-                             int head_chunk, int64_t seq_trunk, int pass, int kv_on_host);
+                             int head_chunk, int64_t seq_trunk, int pass, int host_mask);
 
 /*
  * Forward: o = softmax(scale q k^T + mask) v, lse = ln(sum exp(...)).
- *   q [B,S,Hq,D] bf16 (device); k, v [B,S,Hkv,D] bf16 (device, or both pinned host);
- *   o [B,S,Hq,D] bf16 (device, written); lse [B,Hq,S] float32 (device, written), or NULL
- *     for a prefill (inference) call that keeps no softmax statistics: then only o is
- *     written, by the same kernels.
+ *   q [B,S,Hq,D] bf16 (device or pinned host); k, v [B,S,Hkv,D] bf16 (device, or both pinned
+ *     host); o [B,S,Hq,D] bf16 (device or pinned host, written); lse [B,Hq,S] float32
+ *     (device, written), or NULL for a prefill (inference) call that keeps no softmax
+ *     statistics: then only o is written, by the same kernels. A host q is copied in one head
+ *     group at a time on the library's copy stream while the previous group computes, and a
+ *     host o is copied out one group at a time while the next group computes ("Training Ultra
+ *     Long Context LM with Fully Pipelined Distributed Transformer", Key Findings: host
+ *     offload with double buffering); the caller's stream completes after the last copy.
  *   causal: 1 = key j visible to query i iff j <= i; 0 = full attention.
  *   head_chunk: q-heads per group; must divide Hq and be a multiple of Hq/Hkv (a group owns
  *     whole kv-heads). head_chunk = Hq is the unchunked schedule.
  *   seq_trunk: trunk length T in tokens. T >= S means one trunk; otherwise T % 128 == 0.
  *     The last trunk may be shorter (ragged).
- *   workspace: device buffer of >= upipe_workspace_bytes(..., UPIPE_PASS_FWD, kv_on_host)
- *     bytes, 256-byte aligned; contents on entry are ignored and on exit are undefined.
+ *   workspace: device buffer of >= upipe_workspace_bytes(..., UPIPE_PASS_FWD, host_mask)
+ *     bytes for the placement of this call, 256-byte aligned; contents on entry are ignored
+ *     and on exit are undefined.
  *   Supported: D in {64, 128}; any S >= 1; B, Hq, Hkv >= 1 (UNSUPPORTED otherwise).
  */
 int upipe_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -123,7 +136,7 @@ int upipe_attn_bwd(const void* q, const void* k, const void* v, const void* o,
  *   - The forward's scratch is a file-scope static device array of 32 MiB, created when the
  *     library's device code is loaded on a GPU and held by every GPU that loads it until the
  *     process exits. Problems whose forward workspace (upipe_workspace_bytes, UPIPE_PASS_FWD,
- *     kv_on_host = 0) exceeds 32 MiB are rejected with UPIPE_ERR_WORKSPACE_TOO_SMALL; e.g. the
+ *     host_mask = 0) exceeds 32 MiB are rejected with UPIPE_ERR_WORKSPACE_TOO_SMALL; e.g. the
  *     Llama3-8B-shaped layer fits up to S = 8192 with head_chunk = 8.
  *   - No call allocates or frees anything (no cudaMalloc/cudaFree, no allocating library call).
  *   - The first call on a device does the per-device set-up (looks up the array's device

@@ -34,7 +34,7 @@ def test_library_exports_every_declared_symbol():
     assert set(declared_functions()) == set(up.SIGNATURES), "binding and header disagree"
 
 
-def _expected_ws(B, S, Hq, Hkv, D, hc, T, kv_host):
+def _expected_ws(B, S, Hq, Hkv, D, hc, T, kv_host, act_host=False):
     """The workspace arena as documented: every segment 256-byte aligned."""
     al = lambda x: (x + 255) // 256 * 256  # noqa: E731
     G = Hq // Hkv
@@ -45,7 +45,7 @@ def _expected_ws(B, S, Hq, Hkv, D, hc, T, kv_host):
     ntr = (S + T - 1) // T
     qw = B * hc * S * D * 2
     kv = 4 * al(B * kc * T * D * 2) if kv_host else 2 * al(B * kc * S * D * 2)
-    fwd = al(qw) + kv
+    fwd = al(qw) + kv + (3 * al(qw) if act_host else 0)  # host q/o: Q buffer 2, 2 O stagings
     if ntr > 1:  # running state: every query trunk's rows with host K/V, one trunk's otherwise
         rows = S_pad if kv_host else T_pad
         fwd += al(B * hc * rows * D * 4) + al(B * hc * rows * 8)
@@ -53,6 +53,8 @@ def _expected_ws(B, S, Hq, Hkv, D, hc, T, kv_host):
     # pinned host memory as well)
     dkdv = 4 * al(B * kc * T * D * 2) if kv_host else 0
     bwd = 2 * al(qw) + kv + dkdv + al(B * hc * S_pad * D * 4) + 2 * al(B * hc * S_pad * 4)
+    if act_host:  # host q/o/dout/dq: Q and dO buffer 2, 2 head-major O copies, 2 dQ stagings
+        bwd += 6 * al(qw)
     return fwd, bwd
 
 
@@ -151,3 +153,19 @@ def test_launch_count_and_profile_read_without_gpu():
     up.upipe_profile_enable(False)
     stats = up.upipe_profile_read()
     assert set(stats) == set(up.KERNEL_CLASSES)
+
+
+@pytest.mark.parametrize("name", WORKLOAD_ORDER)
+def test_workspace_with_host_activations(name):
+    """UPIPE_HOST_ACT adds head-group-sized staging only, so the chunked/unchunked ratio holds."""
+    w = WORKLOADS[name]
+    mask = (up.UPIPE_HOST_KV if w.kv_on_host else 0) | up.UPIPE_HOST_ACT
+    fwd, bwd = _expected_ws(w.B, w.S, w.Hq, w.Hkv, w.D, w.head_chunk, w.seq_trunk, w.kv_on_host,
+                            act_host=True)
+    args = (w.B, w.S, w.Hq, w.Hkv, w.D, 1, w.head_chunk, w.seq_trunk)
+    assert up.upipe_workspace_bytes(*args, up.UPIPE_PASS_FWD, mask) == fwd
+    assert up.upipe_workspace_bytes(*args, up.UPIPE_PASS_BWD, mask) == bwd
+    full = up.upipe_workspace_bytes(w.B, w.S, w.Hq, w.Hkv, w.D, 1, w.Hq, w.seq_trunk,
+                                    up.UPIPE_PASS_BOTH, mask)
+    part = up.upipe_workspace_bytes(*args, up.UPIPE_PASS_BOTH, mask)
+    assert abs(part / full - w.head_chunk / w.Hq) < 1e-3
