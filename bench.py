@@ -53,8 +53,9 @@ def _args():
     ap.add_argument("--seq-trunks", default=None,
                     help="comma-separated seq_trunk values for --sweep (default: per sweep)")
     ap.add_argument("--kv-modes", default=None,
-                    help="for --sweep host-kv: comma-separated subset of device,host,host+dkdv "
-                         "(host+dkdv: dK/dV in pinned host memory as well)")
+                    help="for --sweep host-kv: comma-separated subset of device,host,host+dkdv,all "
+                         "(host+dkdv: dK/dV in pinned host memory as well; all: q, o, dout, dq "
+                         "too)")
     return ap.parse_args()
 
 
@@ -452,10 +453,47 @@ def run_ours(a):
         barrier()
         breakdown = {k: sum(ev[i].elapsed_time(ev[i + 1]) for ev in ph) / a.steps
                      for i, k in enumerate(("h2d_ms", "compute_ms", "d2h_ms"))}
+        e2e_copy_value, _ = job_throughput(e0.elapsed_time(e1), a.steps, f_fwd + f_bwd, world, red)
+        explicit = {"value": e2e_copy_value, "per_step_ms": breakdown,
+                    "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                    "method": "user copies around device-buffer calls; dO in during the forward, "
+                              "O and LSE out during the backward"}
+
+        # The same step through the library with every tensor in pinned host memory: q, k, v,
+        # dout in and o, dq, dk, dv out are staged by the library one head group (and key/value
+        # trunk) at a time while the neighbouring group computes; LSE stays on the device and
+        # is read back at the end of each step.
+        mask = up.UPIPE_HOST_KV | up.UPIPE_HOST_ACT
+        ws_h_bytes = up.upipe_workspace_bytes(B, S, Hq, Hkv, D, 1, hc, T, up.UPIPE_PASS_BOTH, mask)
+        ws_h = torch.empty(ws_h_bytes, dtype=torch.uint8, device=dev)
+        ho, hdq = (torch.empty(q.shape, dtype=q.dtype, pin_memory=True) for _ in range(2))
+        hdk, hdv = (torch.empty(k.shape, dtype=k.dtype, pin_memory=True) for _ in range(2))
+        hlse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+
+        def e2e_host_step():
+            up.upipe_attn_fwd(hq, hk, hv, ho, lse, B, S, Hq, Hkv, D, 1, hc, T, ws_h, ws_h_bytes,
+                              stream)
+            up.upipe_attn_bwd(hq, hk, hv, ho, lse, hdo, hdq, hdk, hdv, B, S, Hq, Hkv, D, 1, hc, T,
+                              ws_h, ws_h_bytes, stream)
+            hlse.copy_(lse, non_blocking=True)
+
+        e2e_host_step()
+        barrier()
+        e0.record(stream)
+        for i in range(a.steps):
+            e2e_host_step()
+        e1.record(stream)
+        barrier()
         e2e_value, _ = job_throughput(e0.elapsed_time(e1), a.steps, f_fwd + f_bwd, world, red)
+        # bytes the library moves per step: the forward reads q, k, v and writes o; the
+        # backward reads q, k, v, o, dout and writes dq, dk, dv; plus the LSE read-back
+        h2d = 2 * (hq.nbytes + hk.nbytes + hv.nbytes) + ho.nbytes + hdo.nbytes
+        d2h = ho.nbytes + hdq.nbytes + hdk.nbytes + hdv.nbytes + hlse.nbytes
         line["e2e"] = {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-                       "d2h_bytes_per_step": int(d2h), "per_step_ms": breakdown,
-                       "overlap": "dO in during the forward, O and LSE out during the backward"}
+                       "d2h_bytes_per_step": int(d2h),
+                       "method": "upipe_attn_fwd/bwd with q, k, v, dout, o, dq, dk, dv in pinned "
+                                 "host memory (library stages them per head group); LSE read back",
+                       "workspace_gb": ws_h_bytes / 1e9, "explicit_copies": explicit}
         up.upipe_sync_status(stream)
 
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
@@ -495,8 +533,16 @@ def run_sweep(a):
                 for T in ints(a.seq_trunks, [a.seq_trunk or w.seq_trunk])]
         kv_modes = (a.kv_modes or "device,host").split(",")
     for mode in kv_modes:
-        kv_host = mode in ("host", "host+dkdv")
-        dkdv_host = mode == "host+dkdv"
+        kv_host = mode in ("host", "host+dkdv", "all")
+        dkdv_host = mode in ("host+dkdv", "all")
+        act_host = mode == "all"  # q, o, dout, dq pinned on the host as well
+        if act_host:
+            qq = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+            qq.copy_(q)
+            ddo = torch.empty(do.shape, dtype=do.dtype, pin_memory=True)
+            ddo.copy_(do)
+        else:
+            qq, ddo = q, do
         if kv_host:
             kk = torch.empty(k.shape, dtype=k.dtype, pin_memory=True)
             kk.copy_(k)
@@ -505,12 +551,17 @@ def run_sweep(a):
         else:
             kk, vv = k, v
         for hc, T in grid:
+            mask = (up.UPIPE_HOST_KV if kv_host else 0) | (up.UPIPE_HOST_ACT if act_host else 0)
             ws_b = up.upipe_workspace_bytes(w.B, w.S, w.Hq, w.Hkv, w.D, 1, hc, T,
-                                            up.UPIPE_PASS_BOTH, kv_host)
+                                            up.UPIPE_PASS_BOTH, mask)
             ws = torch.empty(ws_b, dtype=torch.uint8, device=dev)
-            o = torch.empty_like(q)
+            if act_host:
+                o = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+                dq = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+            else:
+                o = torch.empty_like(q)
+                dq = torch.empty_like(q)
             lse = torch.empty((w.B, w.Hq, w.S), dtype=torch.float32, device=dev)
-            dq = torch.empty_like(q)
             if dkdv_host:
                 dk = torch.empty(k.shape, dtype=k.dtype, pin_memory=True)
                 dv = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
@@ -520,10 +571,10 @@ def run_sweep(a):
             args = (w.B, w.S, w.Hq, w.Hkv, w.D, 1, hc, T)
 
             def fwd():
-                up.upipe_attn_fwd(q, kk, vv, o, lse, *args, ws, ws_b)
+                up.upipe_attn_fwd(qq, kk, vv, o, lse, *args, ws, ws_b)
 
             def bwd():
-                up.upipe_attn_bwd(q, kk, vv, o, lse, do, dq, dk, dv, *args, ws, ws_b)
+                up.upipe_attn_bwd(qq, kk, vv, o, lse, ddo, dq, dk, dv, *args, ws, ws_b)
 
             torch.cuda.synchronize()
             free0 = torch.cuda.mem_get_info()[0]
@@ -548,11 +599,12 @@ def run_sweep(a):
             print(json.dumps({
                 "sweep": a.sweep, "workload": w.name, "S": w.S, "head_chunk": hc,
                 "seq_trunk": T, "kv_on_host": kv_host, "dkdv_on_host": dkdv_host,
+                "activations_on_host": act_host,
                 "fwd_tflops": ff / tf / 1e9,
                 "bwd_tflops": fb / tb / 1e9, "fwdbwd_tflops": (ff + fb) / (tf + tb) / 1e9,
                 "ms_per_step": (tf + tb) / a.steps, "workspace_gb": ws_b / 1e9,
                 "workspace_unchunked_gb": up.upipe_workspace_bytes(
-                    w.B, w.S, w.Hq, w.Hkv, w.D, 1, w.Hq, T, up.UPIPE_PASS_BOTH, kv_host) / 1e9,
+                    w.B, w.S, w.Hq, w.Hkv, w.D, 1, w.Hq, T, up.UPIPE_PASS_BOTH, mask) / 1e9,
                 "device_bytes_allocated_by_calls": int(lib_alloc)}), flush=True)
             del ws
 
