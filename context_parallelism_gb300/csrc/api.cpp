@@ -58,7 +58,8 @@ int cuda_fail(cudaError_t e, const char* what) {
 // ---- per-device state -----------------------------------------------------------------------
 struct DevState {
   bool ready = false;
-  cudaStream_t copy = nullptr;
+  cudaStream_t copy = nullptr;      // key/value trunks in, dK/dV trunks out
+  cudaStream_t act_copy = nullptr;  // head-group activations in and out (bulk, with slack)
   cudaEvent_t slot_ready[2] = {nullptr, nullptr};
   cudaEvent_t slot_free[2] = {nullptr, nullptr};
   cudaEvent_t dkdv_done[2] = {nullptr, nullptr};  // a dK/dV slot is written (compute stream)
@@ -69,6 +70,7 @@ struct DevState {
   cudaEvent_t out_free[2] = {nullptr, nullptr};   // ... and have been copied to the host
   cudaEvent_t entry = nullptr;
   cudaEvent_t copy_done = nullptr;
+  cudaEvent_t act_done = nullptr;
   uint32_t* err = nullptr;  // 256-byte status word allocation
 };
 constexpr int kMaxDev = 64;
@@ -80,6 +82,7 @@ int dev_state(int dev, DevState** out) {
   DevState& d = g_dev[dev];
   if (!d.ready) {
     UPIPE_CUDA(cudaStreamCreateWithFlags(&d.copy, cudaStreamNonBlocking));
+    UPIPE_CUDA(cudaStreamCreateWithFlags(&d.act_copy, cudaStreamNonBlocking));
     for (int i = 0; i < 2; ++i) {
       UPIPE_CUDA(cudaEventCreateWithFlags(&d.slot_ready[i], cudaEventDisableTiming));
       UPIPE_CUDA(cudaEventCreateWithFlags(&d.slot_free[i], cudaEventDisableTiming));
@@ -92,6 +95,7 @@ int dev_state(int dev, DevState** out) {
     }
     UPIPE_CUDA(cudaEventCreateWithFlags(&d.entry, cudaEventDisableTiming));
     UPIPE_CUDA(cudaEventCreateWithFlags(&d.copy_done, cudaEventDisableTiming));
+    UPIPE_CUDA(cudaEventCreateWithFlags(&d.act_done, cudaEventDisableTiming));
     UPIPE_CUDA(cudaMalloc(&d.err, 256));
     UPIPE_CUDA(cudaMemset(d.err, 0, 256));
     UPIPE_CUDA(cudaDeviceSynchronize());
@@ -512,16 +516,17 @@ int upipe_attn_fwd(const void* q, const void* k, const void* v, void* o, float* 
     // The copy stream must not touch the workspace before earlier work on `stream` is done.
     UPIPE_CUDA(cudaEventRecord(ds->entry, stream));
     UPIPE_CUDA(cudaStreamWaitEvent(ds->copy, ds->entry, 0));
+    UPIPE_CUDA(cudaStreamWaitEvent(ds->act_copy, ds->entry, 0));
   }
   const int n_groups = Hq / p.hc;
   auto q_buf = [&](int g) -> uint8_t* { return ws + ((q_host && (g & 1)) ? p.f_qw2 : p.f_qw); };
   // host q: group g's heads go into Q buffer g%2 once group g-2 no longer reads it
   auto stage_q = [&](int g) -> int {
     const int s = g & 1;
-    if (g >= 2) UPIPE_CUDA(cudaStreamWaitEvent(ds->copy, ds->act_free[s], 0));
-    const int r = stage_heads(q, q_buf(g), B, S, Hq, D, g * p.hc, p.hc, ds->copy);
+    if (g >= 2) UPIPE_CUDA(cudaStreamWaitEvent(ds->act_copy, ds->act_free[s], 0));
+    const int r = stage_heads(q, q_buf(g), B, S, Hq, D, g * p.hc, p.hc, ds->act_copy);
     if (r != UPIPE_OK) return r;
-    UPIPE_CUDA(cudaEventRecord(ds->act_ready[s], ds->copy));
+    UPIPE_CUDA(cudaEventRecord(ds->act_ready[s], ds->act_copy));
     return UPIPE_OK;
   };
   if (q_host) {
@@ -616,16 +621,16 @@ int upipe_attn_fwd(const void* q, const void* k, const void* v, void* o, float* 
     if (q_host) UPIPE_CUDA(cudaEventRecord(ds->act_free[gs], stream));
     if (o_host) {
       UPIPE_CUDA(cudaEventRecord(ds->out_done[gs], stream));
-      UPIPE_CUDA(cudaStreamWaitEvent(ds->copy, ds->out_done[gs], 0));
-      st = unstage_heads(ws + p.f_ostg[gs], o, B, S, Hq, D, h0, p.hc, ds->copy);
+      UPIPE_CUDA(cudaStreamWaitEvent(ds->act_copy, ds->out_done[gs], 0));
+      st = unstage_heads(ws + p.f_ostg[gs], o, B, S, Hq, D, h0, p.hc, ds->act_copy);
       if (st != UPIPE_OK) return st;
-      UPIPE_CUDA(cudaEventRecord(ds->out_free[gs], ds->copy));
+      UPIPE_CUDA(cudaEventRecord(ds->out_free[gs], ds->act_copy));
     }
   }
   if (o_host) {
     // the caller's stream completes only after the last group's O reached the host
-    UPIPE_CUDA(cudaEventRecord(ds->copy_done, ds->copy));
-    UPIPE_CUDA(cudaStreamWaitEvent(stream, ds->copy_done, 0));
+    UPIPE_CUDA(cudaEventRecord(ds->act_done, ds->act_copy));
+    UPIPE_CUDA(cudaStreamWaitEvent(stream, ds->act_done, 0));
   }
   return UPIPE_OK;
 }
@@ -712,6 +717,7 @@ int upipe_attn_bwd(const void* q, const void* k, const void* v, const void* o, c
     // The copy stream must not touch the workspace before earlier work on `stream` is done.
     UPIPE_CUDA(cudaEventRecord(ds->entry, stream));
     UPIPE_CUDA(cudaStreamWaitEvent(ds->copy, ds->entry, 0));
+    UPIPE_CUDA(cudaStreamWaitEvent(ds->act_copy, ds->entry, 0));
   }
   const int n_groups = Hq / p.hc;
   // Per head group g, buffers g%2 when host activations rotate through them.
@@ -724,14 +730,15 @@ int upipe_attn_bwd(const void* q, const void* k, const void* v, const void* o, c
   // host q / o / dout: group g's heads are copied head-major once group g-2 is done with them
   auto stage_act = [&](int g) -> int {
     const int s = g & 1, h0 = g * p.hc;
-    if (g >= 2) UPIPE_CUDA(cudaStreamWaitEvent(ds->copy, ds->act_free[s], 0));
+    if (g >= 2) UPIPE_CUDA(cudaStreamWaitEvent(ds->act_copy, ds->act_free[s], 0));
     int r = UPIPE_OK;
-    if (q_host) r = stage_heads(q, qw_of(g), B, S, Hq, D, h0, p.hc, ds->copy);
-    if (r == UPIPE_OK && o_host) r = stage_heads(o, ow_of(g), B, S, Hq, D, h0, p.hc, ds->copy);
+    if (q_host) r = stage_heads(q, qw_of(g), B, S, Hq, D, h0, p.hc, ds->act_copy);
+    if (r == UPIPE_OK && o_host)
+      r = stage_heads(o, ow_of(g), B, S, Hq, D, h0, p.hc, ds->act_copy);
     if (r == UPIPE_OK && dout_host)
-      r = stage_heads(dout, dow_of(g), B, S, Hq, D, h0, p.hc, ds->copy);
+      r = stage_heads(dout, dow_of(g), B, S, Hq, D, h0, p.hc, ds->act_copy);
     if (r != UPIPE_OK) return r;
-    UPIPE_CUDA(cudaEventRecord(ds->act_ready[s], ds->copy));
+    UPIPE_CUDA(cudaEventRecord(ds->act_ready[s], ds->act_copy));
     return UPIPE_OK;
   };
   if (stage_any) {
@@ -823,18 +830,22 @@ int upipe_attn_bwd(const void* q, const void* k, const void* v, const void* o, c
       UPIPE_CUDA(launch_dq_convert(dqacc, ws + p.b_dqs[gs], B, S, p.S_pad, p.hc, D, 0, p.hc,
                                    stream));
       UPIPE_CUDA(cudaEventRecord(ds->out_done[gs], stream));
-      UPIPE_CUDA(cudaStreamWaitEvent(ds->copy, ds->out_done[gs], 0));
-      st = unstage_heads(ws + p.b_dqs[gs], dq, B, S, Hq, D, h0, p.hc, ds->copy);
+      UPIPE_CUDA(cudaStreamWaitEvent(ds->act_copy, ds->out_done[gs], 0));
+      st = unstage_heads(ws + p.b_dqs[gs], dq, B, S, Hq, D, h0, p.hc, ds->act_copy);
       if (st != UPIPE_OK) return st;
-      UPIPE_CUDA(cudaEventRecord(ds->out_free[gs], ds->copy));
+      UPIPE_CUDA(cudaEventRecord(ds->out_free[gs], ds->act_copy));
     } else {
       UPIPE_CUDA(launch_dq_convert(dqacc, dq, B, S, p.S_pad, Hq, D, h0, p.hc, stream));
     }
   }
-  if (dkdv_host || dq_host) {
-    // the caller's stream completes only after the last copy to the host
+  // the caller's stream completes only after the last copy to the host
+  if (dkdv_host) {
     UPIPE_CUDA(cudaEventRecord(ds->copy_done, ds->copy));
     UPIPE_CUDA(cudaStreamWaitEvent(stream, ds->copy_done, 0));
+  }
+  if (dq_host) {
+    UPIPE_CUDA(cudaEventRecord(ds->act_done, ds->act_copy));
+    UPIPE_CUDA(cudaStreamWaitEvent(stream, ds->act_done, 0));
   }
   return UPIPE_OK;
 }
@@ -915,6 +926,8 @@ void upipe_shutdown(void) {
     cudaSetDevice(i);
     cudaStreamSynchronize(d.copy);
     cudaStreamDestroy(d.copy);
+    cudaStreamSynchronize(d.act_copy);
+    cudaStreamDestroy(d.act_copy);
     for (int s = 0; s < 2; ++s) {
       cudaEventDestroy(d.slot_ready[s]);
       cudaEventDestroy(d.slot_free[s]);
@@ -927,6 +940,7 @@ void upipe_shutdown(void) {
     }
     cudaEventDestroy(d.entry);
     cudaEventDestroy(d.copy_done);
+    cudaEventDestroy(d.act_done);
     cudaFree(d.err);
     d = DevState{};
   }

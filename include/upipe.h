@@ -30,7 +30,7 @@
  *   - `stream` is a cudaStream_t (NULL = legacy default stream). All work is enqueued on it
  *     and calls return before the GPU finishes (asynchronous, like a kernel launch).
  *   - Ownership: the caller owns every buffer, including the workspace. Per call the library
- *     allocates no device memory. Per device it lazily creates one internal copy stream,
+ *     allocates no device memory. Per device it lazily creates two internal copy streams,
  *     a few events and a 256-byte device status word; upipe_shutdown() releases them.
  *   - Errors: all arguments are validated before anything is enqueued; on an error nothing
  *     is launched and a status code is returned (see upipe_status). A device-side bounded
@@ -91,7 +91,7 @@ size_t upipe_workspace_bytes(int B, int64_t S, int Hq, int Hkv, int D, int causa
  *     host); o [B,S,Hq,D] bf16 (device or pinned host, written); lse [B,Hq,S] float32
  *     (device, written), or NULL for a prefill (inference) call that keeps no softmax
  *     statistics: then only o is written, by the same kernels. A host q is copied in one head
- *     group at a time on the library's copy stream while the previous group computes, and a
+ *     group at a time on a library copy stream while the previous group computes, and a
  *     host o is copied out one group at a time while the next group computes ("Training Ultra
  *     Long Context LM with Fully Pipelined Distributed Transformer", Key Findings: host
  *     offload with double buffering); the caller's stream completes after the last copy.
