@@ -1,0 +1,126 @@
+"""fp64 CPU oracle for the sequence-tiled per-token loss: the language-model readout
+(hidden state times the vocabulary matrix) followed by token-level cross-entropy.
+
+TEST INFRASTRUCTURE ONLY. Nothing on the product path imports, calls or links this module:
+only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg use it.
+It shares no code with the CUDA path; both take their inputs from ``workloads``.
+
+What it computes. The pages name sequence tiling as the step that chunks the per-token
+("element-wise along the sequence") computations, the loss among them, so that no buffer
+with the whole sequence along one dimension is ever created ["Road to 5 million sequence
+length" talk notes, the Arctic sequence-tiling passage; "Road to 5 Million Tokens" summary,
+§2 item 5, "Sequence Tiling"]. Tiling does not change the result: every token's loss
+depends on that token alone. So the oracle is the plain, untiled definition:
+
+    logits[i, j] = <h_i, w_j>                          (i < S tokens, j < V vocabulary rows)
+    lse[i]       = log sum_j exp(logits[i, j])         (natural log)
+    loss[i]      = lse[i] - logits[i, target[i]]       (0 where target[i] < 0: ignored token)
+
+and, for an upstream gradient g[i] = d(total)/d(loss[i]),
+
+    dlogits[i, j] = g[i] * (softmax(logits[i])_j - [j == target[i]])   (row 0 if ignored)
+    dh[i]         = sum_j dlogits[i, j] * w_j
+    dw[j]         = sum_i dlogits[i, j] * h_i
+
+Readings where the pages are silent: the loss is next-token cross-entropy over the logits of
+a linear readout (the buffer the pages call huge is the S x V logits); a negative target
+marks a token that takes no loss and no gradient (padding); lse and loss are returned per
+token, and the caller's reduction (mean, sum) enters only through g.
+
+Layouts: h [S, Dm], w [V, Dm], target [S] integers, loss / lse / g [S], dh [S, Dm],
+dw [V, Dm]. Arithmetic is numpy float64 on exactly upcast inputs; the logits are formed
+``block`` rows at a time only to bound memory (each row is independent, so the blocking
+cannot change any value).
+
+Parity status: every public function here is pinned by tests/test_oracle_seqtile.py (finite
+differences, closed forms, a logistic-loss special case, scipy's logsumexp, invariants).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = ["ce_loss_ref", "ce_loss_bwd_ref", "ce_rows_ref"]
+
+
+def _f64(x):
+    """Exact upcast to a float64 numpy array (bf16 -> fp32 -> fp64 are exact)."""
+    if hasattr(x, "detach"):
+        t = x.detach()
+        if t.is_floating_point() and t.element_size() < 4:
+            t = t.float()
+        return t.cpu().numpy().astype(np.float64, copy=False)
+    return np.asarray(x, dtype=np.float64)
+
+
+def _i64(x):
+    if hasattr(x, "detach"):
+        return x.detach().cpu().numpy().astype(np.int64, copy=False)
+    return np.asarray(x, dtype=np.int64)
+
+
+def _row_stats(logits, tgt):
+    """lse and loss of a block of logit rows (max-shifted log-sum-exp, natural log)."""
+    m = logits.max(axis=1)
+    lse = m + np.log(np.exp(logits - m[:, None]).sum(axis=1))
+    valid = tgt >= 0
+    picked = np.where(valid, logits[np.arange(len(tgt)), np.where(valid, tgt, 0)], 0.0)
+    loss = np.where(valid, lse - picked, 0.0)
+    return lse, loss
+
+
+def ce_loss_ref(h, w, target, block: int = 512):
+    """Forward: per-token (loss, lse), each float64 [S]."""
+    H, W, t = _f64(h), _f64(w), _i64(target)
+    S = H.shape[0]
+    lse = np.empty(S)
+    loss = np.empty(S)
+    for r0 in range(0, S, block):
+        r1 = min(S, r0 + block)
+        lse[r0:r1], loss[r0:r1] = _row_stats(H[r0:r1] @ W.T, t[r0:r1])
+    return loss, lse
+
+
+def ce_loss_bwd_ref(h, w, target, g, block: int = 512):
+    """Forward and backward: (loss, lse, dh, dw), float64, dh [S, Dm], dw [V, Dm]."""
+    H, W, t, G = _f64(h), _f64(w), _i64(target), _f64(g)
+    S = H.shape[0]
+    lse = np.empty(S)
+    loss = np.empty(S)
+    dh = np.empty_like(H)
+    dw = np.zeros_like(W)
+    for r0 in range(0, S, block):
+        r1 = min(S, r0 + block)
+        logits = H[r0:r1] @ W.T
+        tb = t[r0:r1]
+        lse[r0:r1], loss[r0:r1] = _row_stats(logits, tb)
+        p = np.exp(logits - lse[r0:r1, None])          # softmax rows
+        valid = tb >= 0
+        rows = np.nonzero(valid)[0]
+        p[rows, tb[rows]] -= 1.0
+        p *= np.where(valid, G[r0:r1], 0.0)[:, None]    # dlogits
+        dh[r0:r1] = p @ W
+        dw += p.T @ H[r0:r1]
+    return loss, lse, dh, dw
+
+
+def ce_rows_ref(h, w, target, g, rows):
+    """loss, lse and dh at the given token rows only (each row needs only its own logits):
+    the check used where the whole problem is too large for the CPU."""
+    rows = np.asarray(rows, dtype=np.int64)
+    if hasattr(h, "detach"):
+        import torch
+        idx = torch.as_tensor(rows, device=h.device)
+        H = _f64(h[idx])
+        t = _i64(target[idx])
+        G = _f64(g[idx])
+    else:
+        H, t, G = _f64(h)[rows], _i64(target)[rows], _f64(g)[rows]
+    W = _f64(w)
+    logits = H @ W.T
+    lse, loss = _row_stats(logits, t)
+    p = np.exp(logits - lse[:, None])
+    valid = t >= 0
+    vr = np.nonzero(valid)[0]
+    p[vr, t[vr]] -= 1.0
+    p *= np.where(valid, G, 0.0)[:, None]
+    return loss, lse, p @ W
