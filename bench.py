@@ -11,6 +11,10 @@ GPU (the path does not shard on one box); value = total FLOPs of all ranks / max
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                   [--head-chunk H] [--seq-trunk T] [--impl ours|reference]
+
+--workload llama8b_readout_s128k (or readout_small) measures the sequence-tiled readout +
+cross-entropy loss instead (one step = upipe_ce_fwd + upipe_ce_bwd over S tokens, seq_tile
+tokens at a time; FLOPs: fwd 2*S*V*Dm, bwd 3x that) and prints its own JSON line.
 """
 from __future__ import annotations
 
@@ -39,6 +43,8 @@ def _args():
     ap.add_argument("--workload", default="llama8b_s128k")
     ap.add_argument("--head-chunk", type=int, default=None)
     ap.add_argument("--seq-trunk", type=int, default=None)
+    ap.add_argument("--seq-tile", type=int, default=None,
+                    help="tokens per tile for the loss workloads (default: the workload's)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -609,8 +615,204 @@ def run_sweep(a):
             del ws
 
 
+LOSS_METRIC = "sequence-tiled readout + cross-entropy fwd+bwd TFLOP/s on 1 GB300"
+
+
+def loss_oracle_sample(lw, S_sample, inputs):
+    """Times the fp64 oracle's loss forward + backward on the first S_sample tokens (the full
+    vocabulary and width). Returns (tflops, seconds, description, cores)."""
+    import oracle
+    h, w, t, g = inputs
+    hs, ts, gs = h[:S_sample].cpu(), t[:S_sample].cpu(), g[:S_sample].cpu()
+    ws = w.cpu()
+    flops = lw.with_(S=S_sample).flops_fwd() + lw.with_(S=S_sample).flops_bwd()
+    t0 = time.perf_counter()
+    oracle.ce_loss_bwd_ref(hs, ws, ts, gs)
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    desc = (f"fp64 numpy oracle loss fwd+bwd on the first {S_sample} of {lw.S} tokens, full "
+            f"vocabulary {lw.V} x width {lw.Dm}; FLOPs by the same convention")
+    return flops / dt / 1e12, dt, desc, cores
+
+
+def run_loss(a):
+    """The sequence-tiled loss on one GPU (N independent replicas under torchrun)."""
+    import torch
+    import torch.distributed as dist
+
+    import context_parallelism_gb300 as up
+    from workloads import LOSS_WORKLOADS, make_loss_inputs
+
+    rank, world, local = _dist()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    lw = LOSS_WORKLOADS[a.workload]
+    T = a.seq_tile or lw.seq_tile
+    S, Dm, V = lw.S, lw.Dm, lw.V
+    h, w, t, g = (x.to(dev) for x in make_loss_inputs(lw, str(dev) if lw.gen_device == "cuda"
+                                                      else "cpu"))
+    loss = torch.empty(S, dtype=torch.float32, device=dev)
+    lse = torch.empty(S, dtype=torch.float32, device=dev)
+    dh = torch.empty_like(h)
+    dw = torch.empty((V, Dm), dtype=torch.float32, device=dev)
+    ws_bytes = up.upipe_ce_workspace_bytes(S, Dm, V, T, up.UPIPE_PASS_BOTH)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd():
+        up.upipe_ce_fwd(h, w, t, loss, lse, S, Dm, V, T, ws, ws_bytes, stream)
+
+    def bwd():
+        up.upipe_ce_bwd(h, w, t, lse, g, dh, dw, S, Dm, V, T, ws, ws_bytes, stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(a.warmup):
+        fwd()
+        bwd()
+    up.upipe_sync_status(stream)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(a.steps)]
+    up.upipe_profile_read()
+    up.upipe_profile_enable(True)
+    clocks = ClockSampler(local)
+    barrier()
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = up.upipe_launch_count()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(a.steps):
+        ev[i][0].record(stream)
+        fwd()
+        ev[i][1].record(stream)
+        bwd()
+        ev[i][2].record(stream)
+    t1.record(stream)
+    barrier()
+    launches = up.upipe_launch_count() - launches0
+    clk = clocks.stop()
+    up.upipe_profile_enable(False)
+    prof = up.upipe_profile_read()
+    up.upipe_sync_status(stream)
+    fwd_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
+    bwd_ms = sum(e[1].elapsed_time(e[2]) for e in ev)
+    f_fwd, f_bwd = lw.flops_fwd(), lw.flops_bwd()
+    red = torch_reduce_max(dev) if world > 1 else None
+    value, t_max = job_throughput(t0.elapsed_time(t1), a.steps, f_fwd + f_bwd, world, red)
+    peaks, peak_src = _peaks()
+    peak = float(peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"])
+    gemm_ms, gemm_n = prof["loss_gemm"]
+    achieved = (f_fwd + f_bwd) * a.steps / (gemm_ms / 1e3) / 1e12 if gemm_ms > 0 else None
+    roofline = {"kernel": "loss_gemm", "bound": "tensor", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak if achieved else None,
+                "peak_source": f"{peak_src} bf16_tflops_sustained", "launches": gemm_n,
+                "avg_launch_ms": gemm_ms / max(gemm_n, 1),
+                "traffic": traffic_per_launch("loss_gemm", lw.name, T, None),
+                "traffic_unit": "bytes per launch"}
+    kernels = {k: {"ms_per_step": tm / a.steps, "launches_per_step": n / a.steps}
+               for k, (tm, n) in prof.items() if n}
+    line = {
+        "metric": LOSS_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": t_max / a.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded: h N(0,1), w N(0,%g/sqrt(Dm)) bf16, uniform targets, "
+                "%.4f ignored)" % (lw.w_std, lw.ignore_frac),
+        "config": {"workload": lw.name, "S": S, "Dm": Dm, "V": V, "seq_tile": T,
+                   "l2": "inputs larger than L2 (w is %.2f GiB)" % (w.nbytes / 2**30),
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "fwd_tflops": world * f_fwd * a.steps / (fwd_ms / 1e3) / 1e12,
+        "bwd_tflops": world * f_bwd * a.steps / (bwd_ms / 1e3) / 1e12,
+        "frac_of_bf16_peak": value / world / peak, "peak_tflops": peak,
+        "workspace_gb": ws_bytes / 1e9,
+        "untiled_logits_gb": S * V * 4 / 1e9,
+        "roofline": roofline, "kernels": kernels, "gpu_launches": int(launches), "clocks": clk,
+    }
+    if not a.no_e2e:
+        # host buffers in (h, w, target, dloss), loss / lse / dh / dw out, every step
+        hh = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (h, w, t, g)]
+        for src, dst in zip((h, w, t, g), hh):
+            dst.copy_(src)
+        outs = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (loss, lse, dh, dw)]
+
+        def e2e_step():
+            for dst, src in zip((h, w, t, g), hh):
+                dst.copy_(src, non_blocking=True)
+            fwd()
+            bwd()
+            for dst, src in zip(outs, (loss, lse, dh, dw)):
+                dst.copy_(src, non_blocking=True)
+
+        e2e_step()
+        barrier()
+        t0.record(stream)
+        for _ in range(a.steps):
+            e2e_step()
+        t1.record(stream)
+        barrier()
+        e2e_value, _ = job_throughput(t0.elapsed_time(t1), a.steps, f_fwd + f_bwd, world, red)
+        line["e2e"] = {"value": e2e_value, "unit": UNIT,
+                       "h2d_bytes_per_step": int(sum(x.nbytes for x in hh)),
+                       "d2h_bytes_per_step": int(sum(x.nbytes for x in outs)),
+                       "method": "pinned host h, w, target, dloss copied in and loss, lse, dh, dw "
+                                 "copied out on the compute stream around upipe_ce_fwd/bwd"}
+        up.upipe_sync_status(stream)
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        tf, dt, desc, cores = loss_oracle_sample(lw, min(S, 32), (h, w, t, g))
+        line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": desc, "seconds": dt}
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_loss_reference(a):
+    """Reference arm for the loss workloads: the fp64 oracle on the host cores, rank 0 only."""
+    rank, _, _ = _dist()
+    if rank != 0:
+        return
+    from workloads import LOSS_WORKLOADS, make_loss_inputs
+    lw = LOSS_WORKLOADS[a.workload]
+    S_sample = min(lw.S, 32)
+    inputs = make_loss_inputs(lw.with_(S=S_sample, gen_device="cpu"), "cpu")
+    # the sample regenerates the recipe at the sample length: same shapes and distributions
+    vals = []
+    for i in range(a.warmup + a.steps):
+        tf, dt, desc, cores = loss_oracle_sample(lw, S_sample, inputs)
+        if i >= a.warmup:
+            vals.append(dt)
+    flops = lw.with_(S=S_sample).flops_fwd() + lw.with_(S=S_sample).flops_bwd()
+    value = flops * len(vals) / sum(vals) / 1e12
+    line = {
+        "impl": "reference", "metric": LOSS_METRIC, "value": value, "unit": UNIT,
+        "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": 1000.0 * statistics.mean(vals), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": lw.name, "S": lw.S, "Dm": lw.Dm, "V": lw.V,
+                   "seq_tile": a.seq_tile or lw.seq_tile, "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc + " (recipe regenerated on the CPU at the sample length)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     a = _args()
+    from workloads import LOSS_WORKLOADS
+    if a.workload in LOSS_WORKLOADS:
+        if a.impl == "reference":
+            run_loss_reference(a)
+        else:
+            run_loss(a)
+        return
     if a.sweep:
         run_sweep(a)
         return

@@ -27,7 +27,8 @@ UPIPE_ERR_TIMEOUT = 5
 UPIPE_PASS_FWD, UPIPE_PASS_BWD, UPIPE_PASS_BOTH = 0, 1, 2
 UPIPE_HOST_KV, UPIPE_HOST_ACT = 1, 2
 
-KERNEL_CLASSES = ["layout", "attn_fwd", "bwd_pre", "attn_bwd", "dq_convert", "other"]
+KERNEL_CLASSES = ["layout", "attn_fwd", "bwd_pre", "attn_bwd", "dq_convert", "other",
+                  "loss_gemm", "loss_merge"]
 
 # Every symbol include/upipe.h declares, with (restype, argtypes).
 _vp, _i, _i64, _sz, _u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_uint64
@@ -56,6 +57,10 @@ SIGNATURES = {
     "upipe_profile_read": (_i, [ctypes.POINTER(KernelStat), _i]),
     "upipe_selftest_umma": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp]),
     "upipe_selftest_wait_timeout": (_i, [_i, _vp]),
+    "upipe_ce_workspace_bytes": (_sz, [_i64, _i, _i64, _i64, _i]),
+    "upipe_ce_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i64, _i, _i64, _i64, _vp, _sz, _vp]),
+    "upipe_ce_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i, _i64, _i64, _vp, _sz,
+                          _vp]),
 }
 
 
@@ -203,6 +208,27 @@ def upipe_selftest_wait_timeout(limit_us, stream=None):
            "upipe_selftest_wait_timeout")
 
 
+def upipe_ce_workspace_bytes(S, Dm, V, seq_tile, pass_=UPIPE_PASS_BOTH):
+    return int(_lib.upipe_ce_workspace_bytes(S, Dm, V, seq_tile, pass_))
+
+
+def upipe_ce_fwd(h, w, target, loss, lse, S, Dm, V, seq_tile, workspace, workspace_bytes=None,
+                 stream=None):
+    wb = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    st = _lib.upipe_ce_fwd(_ptr(h), _ptr(w), _ptr(target), _ptr(loss), _ptr(lse), S, Dm, V,
+                           seq_tile, _ptr(workspace), wb, _stream(stream, h, loss, workspace))
+    _check(st, "upipe_ce_fwd")
+
+
+def upipe_ce_bwd(h, w, target, lse, dloss, dh, dw, S, Dm, V, seq_tile, workspace,
+                 workspace_bytes=None, stream=None):
+    wb = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    st = _lib.upipe_ce_bwd(_ptr(h), _ptr(w), _ptr(target), _ptr(lse), _ptr(dloss), _ptr(dh),
+                           _ptr(dw), S, Dm, V, seq_tile, _ptr(workspace), wb,
+                           _stream(stream, h, dh, workspace))
+    _check(st, "upipe_ce_bwd")
+
+
 # ---- convenience: allocate outputs / workspace with torch, then call the ABI -------------
 
 def _dims(q, k):
@@ -279,3 +305,38 @@ def attention_backward(q, k, v, o, lse, dout, causal=True, head_chunk=None, seq_
     upipe_attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, S, Hq, Hkv, D, causal, hc, T, workspace,
                    None, stream)
     return dq, dk, dv
+
+
+def ce_loss_forward(h, w, target, seq_tile=8192, workspace=None, stream=None):
+    """loss, lse (float32 [S]) of the readout h [S, Dm] @ w[V, Dm]^T followed by token-level
+    cross-entropy against target [S] (int64, negative = ignored), computed seq_tile tokens at
+    a time without storing logits."""
+    import torch
+    S, Dm = h.shape
+    V = w.shape[0]
+    loss = torch.empty(S, dtype=torch.float32, device=h.device)
+    lse = torch.empty(S, dtype=torch.float32, device=h.device)
+    need = upipe_ce_workspace_bytes(S, Dm, V, seq_tile, UPIPE_PASS_FWD)
+    if need == 0:
+        upipe_ce_fwd(h, w, target, loss, lse, S, Dm, V, seq_tile, 0, 0, stream)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=h.device)
+    upipe_ce_fwd(h, w, target, loss, lse, S, Dm, V, seq_tile, workspace, None, stream)
+    return loss, lse
+
+
+def ce_loss_backward(h, w, target, lse, dloss, seq_tile=8192, workspace=None, stream=None):
+    """dh (bf16 [S, Dm]) and dw (float32 [V, Dm]) of sum_i dloss[i] * loss[i] for the forward
+    above; lse is the forward's."""
+    import torch
+    S, Dm = h.shape
+    V = w.shape[0]
+    dh = torch.empty((S, Dm), dtype=h.dtype, device=h.device)
+    dw = torch.empty((V, Dm), dtype=torch.float32, device=h.device)
+    need = upipe_ce_workspace_bytes(S, Dm, V, seq_tile, UPIPE_PASS_BWD)
+    if need == 0:
+        upipe_ce_bwd(h, w, target, lse, dloss, dh, dw, S, Dm, V, seq_tile, 0, 0, stream)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=h.device)
+    upipe_ce_bwd(h, w, target, lse, dloss, dh, dw, S, Dm, V, seq_tile, workspace, None, stream)
+    return dh, dw

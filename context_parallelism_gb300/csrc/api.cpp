@@ -436,6 +436,17 @@ struct Stager {
 };
 
 }  // namespace
+
+int device_status_word(int dev, uint32_t** err) {
+  if (dev < 0 || dev >= kMaxDev) return fail(UPIPE_ERR_INVALID_ARG, "device %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevState* ds = nullptr;
+  const int st = dev_state(dev, &ds);
+  if (st != UPIPE_OK) return st;
+  *err = ds->err;
+  return UPIPE_OK;
+}
+
 }  // namespace upipe
 
 using namespace upipe;

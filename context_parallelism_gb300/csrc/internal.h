@@ -109,6 +109,42 @@ cudaError_t launch_bwd_pre(const void* o, const void* dout, const float* lse, vo
 cudaError_t launch_dq_convert(const float* dqacc, void* dq, int B, int64_t S, int64_t S_pad,
                               int out_heads, int D, int out_head0, int hc, cudaStream_t stream);
 
+// ---- sequence-tiled loss (gemm_tc.cu) ------------------------------------------------------
+// C[m, n] = sum_k A(m, k) B(n, k) over 128 x 256 tiles, with the epilogue chosen by `epi`.
+enum : int { kEpiCeFwd = 0, kEpiCeBwd = 1, kEpiStoreBf16 = 2, kEpiAccF32 = 3 };
+
+struct GemmArgs {
+  int M, N, K;            // N % 64 == 0; M, K any (tensor maps zero-fill past the edges)
+  int m_fastest;          // tile order: 1 walks M tiles first (shares a B strip), 0 N tiles first
+  void* c;                // STORE: bf16 [M][ldc]; ACC_F32: fp32 [M][ldc]; CE_BWD: bf16 dlogits
+  int64_t ldc;
+  int accumulate;         // ACC_F32: add into c instead of overwriting
+  const int64_t* target;  // CE: [M] vocabulary index of each row's target, < 0 = ignored
+  const float* lse;       // CE_BWD: [M] natural-log log-sum-exp of each row's logits
+  const float* g;         // CE_BWD: [M] upstream gradient of each row's loss
+  float* part;            // CE_FWD: float2 [ceil(N/256)][part_stride] (max in log2 units, sum)
+  int64_t part_stride;
+  float* tlogit;          // CE_FWD: [M] logit at the target
+  uint32_t* err;
+};
+
+// Supported (epi, A MN-major, B MN-major): (CE_FWD, 0, 0), (CE_BWD, 0, 0), (STORE, 0, 1),
+// (ACC_F32, 1, 1). K-major maps have 128-row (A) / 256-row (B) boxes; MN-major maps 64-row
+// boxes; all 64 columns wide with 128-byte swizzle. The grid is min(tiles, grid_cap) CTAs.
+cudaError_t launch_gemm_tc(int epi, bool a_mn, bool b_mn, const CUtensorMap& ta,
+                           const CUtensorMap& tb, const GemmArgs& a, int grid_cap,
+                           cudaStream_t stream);
+
+// loss[r], lse[r] for r < M from the CE_FWD partials of n_parts column tiles (V: vocabulary
+// size, for the out-of-range target check).
+cudaError_t launch_ce_merge(const float* part, int64_t part_stride, int n_parts,
+                            const float* tlogit, const int64_t* target, float* loss, float* lse,
+                            int64_t M, int64_t V, cudaStream_t stream);
+
+// ---- services of api.cpp to the other entry points -----------------------------------------
+// Per-device state (streams, status word) for `dev`, created on first use; a upipe status.
+int device_status_word(int dev, uint32_t** err);
+
 // ---- self-tests (selftest.cu) --------------------------------------------------------------
 cudaError_t launch_selftest_umma(const void* a, const void* b, float* c, int N, int K,
                                  int a_mn, int b_mn, int a_manual, int lbo, int sbo,

@@ -181,6 +181,41 @@ const char* upipe_last_error_message(void);
 /* Releases the per-device copy streams, events and status words. Optional at exit. */
 void upipe_shutdown(void);
 
+/* ---- Sequence tiling: language-model readout + cross-entropy loss ----------------------
+ *
+ * The per-token loss is computed seq_tile tokens at a time, so that no buffer has the whole
+ * sequence along one dimension ("Road to 5 million sequence length" talk notes, Arctic
+ * sequence-tiling passage: element-wise computations such as the loss are chunked along the
+ * sequence; "Road to 5 Million Tokens" summary, section 2 item 5, "Sequence Tiling").
+ * Definition, for tokens i < S and vocabulary rows j < V:
+ *   logits[i][j] = <h_i, w_j>;   lse[i] = ln sum_j exp(logits[i][j]);
+ *   loss[i] = lse[i] - logits[i][target[i]], and 0 when target[i] < 0 (an ignored token);
+ *   backward, for g[i] = d(total)/d(loss[i]) (the caller's reduction, e.g. 1/count for a mean):
+ *   dlogits[i][j] = g[i] (exp(logits[i][j] - lse[i]) - [j == target[i]]) (0 for ignored rows);
+ *   dh = dlogits w;   dw = dlogits^T h.
+ * The forward stores no logits: each 256-column vocabulary tile leaves a (max, sum) pair per
+ * token, merged afterwards. The backward recomputes the logits of one tile of tokens, keeps
+ * that tile's dlogits (bf16, seq_tile x V) in the workspace and consumes it in two GEMMs.
+ * All GEMMs run on the tensor cores (bf16 operands, fp32 accumulation).
+ *
+ * Layouts (dense row-major): h [S][Dm] bf16, w [V][Dm] bf16, target [S] int64, loss, lse and
+ * dloss [S] float32, dh [S][Dm] bf16, dw [V][Dm] float32 (overwritten with the sum over all
+ * tokens). Every pointer: device memory of one device, 16-byte aligned. UPIPE_ERR_UNSUPPORTED
+ * unless Dm % 64 == 0, V % 64 == 0, V < 2^31 and seq_tile % 128 == 0; S >= 1 (the last tile
+ * may be ragged). A target >= V makes that token's loss (and, in the backward, every
+ * gradient) NaN. Workspace: upipe_ce_workspace_bytes (pass as for attention; 0 for a shape
+ * the calls reject): forward ceil(V/256) * T' * 8 + T' * 4 bytes with T' = min(seq_tile, S)
+ * rounded up to 128; backward min(seq_tile, S) * V * 2 bytes; each rounded up to 256.
+ * Asynchronous on `stream`, like the attention calls.
+ */
+size_t upipe_ce_workspace_bytes(int64_t S, int Dm, int64_t V, int64_t seq_tile, int pass);
+int upipe_ce_fwd(const void* h, const void* w, const int64_t* target, float* loss, float* lse,
+                 int64_t S, int Dm, int64_t V, int64_t seq_tile, void* workspace,
+                 size_t workspace_bytes, void* stream);
+int upipe_ce_bwd(const void* h, const void* w, const int64_t* target, const float* lse,
+                 const float* dloss, void* dh, float* dw, int64_t S, int Dm, int64_t V,
+                 int64_t seq_tile, void* workspace, size_t workspace_bytes, void* stream);
+
 /* ---- Diagnostics ---------------------------------------------------------------------- */
 
 /* Kernel classes for launch counting and profiling. */
@@ -191,7 +226,9 @@ enum {
   UPIPE_K_ATTN_BWD = 3,   /* backward attention kernel */
   UPIPE_K_DQ_CONVERT = 4, /* dq float32 -> bf16 token-major */
   UPIPE_K_OTHER = 5,      /* self-tests */
-  UPIPE_K_COUNT = 6
+  UPIPE_K_LOSS_GEMM = 6,  /* sequence-tiled loss: tensor-core GEMMs with their epilogues */
+  UPIPE_K_LOSS_MERGE = 7, /* sequence-tiled loss: per-token merge of the vocabulary tiles */
+  UPIPE_K_COUNT = 8
 };
 
 typedef struct {

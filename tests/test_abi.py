@@ -169,3 +169,50 @@ def test_workspace_with_host_activations(name):
                                     up.UPIPE_PASS_BOTH, mask)
     part = up.upipe_workspace_bytes(*args, up.UPIPE_PASS_BOTH, mask)
     assert abs(part / full - w.head_chunk / w.Hq) < 1e-3
+
+
+# ---- sequence-tiled loss ------------------------------------------------------------------
+
+def _expected_ce_ws(S, Dm, V, T):
+    al = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    Tt = min(T, S)
+    Tp = (Tt + 127) // 128 * 128
+    n_vt = (V + 255) // 256
+    fwd = al(n_vt * Tp * 8) + al(Tp * 4)
+    bwd = al(Tt * V * 2)
+    return fwd, bwd
+
+
+@pytest.mark.parametrize("S,Dm,V,T", [(131072, 4096, 128256, 8192), (1000, 256, 1088, 256),
+                                      (1, 64, 64, 128), (300, 64, 320, 1024)])
+def test_loss_workspace_matches_formula(S, Dm, V, T):
+    fwd, bwd = _expected_ce_ws(S, Dm, V, T)
+    assert up.upipe_ce_workspace_bytes(S, Dm, V, T, up.UPIPE_PASS_FWD) == fwd
+    assert up.upipe_ce_workspace_bytes(S, Dm, V, T, up.UPIPE_PASS_BWD) == bwd
+    assert up.upipe_ce_workspace_bytes(S, Dm, V, T, up.UPIPE_PASS_BOTH) == max(fwd, bwd)
+
+
+def test_loss_workspace_is_bounded_by_the_tile_not_the_sequence():
+    # the point of sequence tiling: the dlogits block depends on seq_tile, not on S
+    a = up.upipe_ce_workspace_bytes(131072, 4096, 128256, 8192, up.UPIPE_PASS_BWD)
+    b = up.upipe_ce_workspace_bytes(1 << 22, 4096, 128256, 8192, up.UPIPE_PASS_BWD)
+    assert a == b == 8192 * 128256 * 2
+
+
+@pytest.mark.parametrize("S,Dm,V,T", [(0, 64, 64, 128), (128, 96, 64, 128), (128, 64, 100, 128),
+                                      (128, 64, 64, 100), (128, 64, 1 << 31, 128)])
+def test_loss_workspace_zero_for_invalid(S, Dm, V, T):
+    assert up.upipe_ce_workspace_bytes(S, Dm, V, T, up.UPIPE_PASS_BOTH) == 0
+
+
+def test_loss_calls_validate_before_device_access():
+    lib = ctypes.CDLL(up.LIB_PATH)
+    st = up._lib.upipe_ce_fwd(None, None, None, None, None, 128, 64, 64, 128, None, 0, None)
+    assert st == up.UPIPE_ERR_INVALID_ARG
+    st = up._lib.upipe_ce_fwd(None, None, None, None, None, 128, 96, 64, 128, None, 0, None)
+    assert st == up.UPIPE_ERR_UNSUPPORTED
+    st = up._lib.upipe_ce_bwd(None, None, None, None, None, None, None, 128, 64, 64, 128, None,
+                              0, None)
+    assert st == up.UPIPE_ERR_INVALID_ARG
+    assert "NULL" in up.upipe_last_error_message()
+    assert lib is not None

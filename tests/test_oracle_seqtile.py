@@ -147,3 +147,10 @@ def test_blocking_and_sampled_rows_agree_with_whole_problem():
     assert np.allclose(loss, b[0][rows], rtol=0, atol=1e-13)
     assert np.allclose(lse, b[1][rows], rtol=0, atol=1e-13)
     assert np.allclose(dh, b[2][rows], rtol=0, atol=1e-13)
+    # with g zero off the sampled rows, their share of dw is all of dw
+    gs = np.zeros_like(g)
+    gs[rows] = g[rows]
+    vr = [0, 5, 17, 39]
+    _, _, _, dw_full = ce_loss_bwd_ref(h, w, t, gs)
+    _, _, _, dw_part = ce_rows_ref(h, w, t, gs, rows, vocab_rows=vr)
+    assert np.allclose(dw_part, dw_full[vr], rtol=0, atol=1e-13)

@@ -150,3 +150,64 @@ def sample_rows(S: int, seq_trunk: int, n: int, seed: int):
     gen = torch.Generator().manual_seed(seed)
     extra = torch.randint(0, S, (max(0, n - len(fixed)),), generator=gen).tolist()
     return sorted(set(fixed) | set(extra))
+
+
+# ---- sequence-tiled loss (readout + cross-entropy) ----------------------------------------
+
+@dataclass(frozen=True)
+class LossWorkload:
+    """A language-model readout + token-level cross-entropy problem.
+
+    Recipe: from ONE ``torch.Generator`` seeded with ``seed``, in this order: h [S, Dm] as
+    standard normals (fp32, rounded to bf16; the scale of a normalised final hidden state),
+    w [V, Dm] as normals of std ``w_std / sqrt(Dm)`` rounded to bf16 (logits of std about
+    ``w_std``), target [S] uniform in [0, V), then a Bernoulli(``ignore_frac``) mask that sets
+    the target of masked tokens to -1 (ignored: padding). The upstream gradient is the mean
+    over the counted tokens, 1 / #(target >= 0), for every counted token.
+    Shapes stand in for a Llama3-8B-shaped model (Dm 4096, vocabulary 128256); no weights
+    are involved."""
+    name: str
+    S: int
+    Dm: int
+    V: int
+    seq_tile: int
+    seed: int
+    w_std: float = 2.0
+    ignore_frac: float = 1.0 / 16
+    gen_device: str = "cpu"
+
+    def flops_fwd(self) -> float:
+        """The readout GEMM, 2 S V Dm (the merge and the epilogues are not counted)."""
+        return 2.0 * self.S * self.V * self.Dm
+
+    def flops_bwd(self) -> float:
+        """Recomputed logits, dh = dlogits w and dw = dlogits^T h: three GEMMs."""
+        return 3.0 * self.flops_fwd()
+
+    def with_(self, **kw) -> "LossWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+LOSS_WORKLOADS = {
+    "readout_small": LossWorkload("readout_small", S=1000, Dm=256, V=1088, seq_tile=256,
+                                  seed=20),
+    "llama8b_readout_s128k": LossWorkload("llama8b_readout_s128k", S=131072, Dm=4096,
+                                          V=128256, seq_tile=8192, seed=21,
+                                          gen_device="cuda"),
+}
+
+
+def make_loss_inputs(lw: LossWorkload, device: str | None = None):
+    """Return (h bf16 [S, Dm], w bf16 [V, Dm], target int64 [S], dloss float32 [S])."""
+    dev = device or lw.gen_device
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(lw.seed)
+    h = _normal_bf16((lw.S, lw.Dm), gen, dev, 1.0)
+    w = _normal_bf16((lw.V, lw.Dm), gen, dev, lw.w_std / math.sqrt(lw.Dm))
+    target = torch.randint(0, lw.V, (lw.S,), generator=gen, device=dev, dtype=torch.int64)
+    if lw.ignore_frac > 0.0:
+        drop = torch.rand((lw.S,), generator=gen, device=dev) < lw.ignore_frac
+        target[drop] = -1
+    n = int((target >= 0).sum().item())
+    dloss = torch.full((lw.S,), 1.0 / max(1, n), dtype=torch.float32, device=dev)
+    return h, w, target, dloss
