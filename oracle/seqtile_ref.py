@@ -103,9 +103,11 @@ def ce_loss_bwd_ref(h, w, target, g, block: int = 512):
     return loss, lse, dh, dw
 
 
-def ce_rows_ref(h, w, target, g, rows):
+def ce_rows_ref(h, w, target, g, rows, vocab_rows=None):
     """loss, lse and dh at the given token rows only (each row needs only its own logits):
-    the check used where the whole problem is too large for the CPU."""
+    the check used where the whole problem is too large for the CPU. With ``vocab_rows``, also
+    the sampled tokens' share of dw at those vocabulary rows, sum_{i in rows} dlogits[i, j] h_i
+    - the whole of dw[j] when g is zero at every other token."""
     rows = np.asarray(rows, dtype=np.int64)
     if hasattr(h, "detach"):
         import torch
@@ -123,4 +125,7 @@ def ce_rows_ref(h, w, target, g, rows):
     vr = np.nonzero(valid)[0]
     p[vr, t[vr]] -= 1.0
     p *= np.where(valid, G, 0.0)[:, None]
-    return loss, lse, p @ W
+    if vocab_rows is None:
+        return loss, lse, p @ W
+    vr = np.asarray(vocab_rows, dtype=np.int64)
+    return loss, lse, p @ W, p[:, vr].T @ H
