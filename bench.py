@@ -78,6 +78,14 @@ TRAFFIC = {
                  "files": ["context_parallelism_gb300/csrc/attn_fwd_pp.cu"],
                  "sha256": "0fc8f248f8edfa9bb850c818a8d0491a4d0934cced9ead929024e61b5c60f791",
                  "bytes": 919404288 + 255160320},
+    # the loss GEMMs (one class, four epilogues): the schedule key is (seq_tile, None); the
+    # figure is the mean over one step's launches - per 8192-token tile the forward logits GEMM
+    # moves 2.20 GB, the backward's recompute 4.27 GB, dh 9.62 GB and dw 11.26 GB
+    "loss_gemm": {"workload": "llama8b_readout_s128k", "head_chunk": 8192, "seq_trunk": None,
+                  "files": ["context_parallelism_gb300/csrc/gemm_tc.cu",
+                            "context_parallelism_gb300/csrc/seqtile_api.cpp"],
+                  "sha256": "e310acce1166d860aa5bf37ccaed437662fc5e5b9a0f95cac746a5d2f2ff3e60",
+                  "bytes": 6836775836},
 }
 
 
@@ -650,6 +658,8 @@ def run_loss(a):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     lw = LOSS_WORKLOADS[a.workload]
+    if a.seq_len:
+        lw = lw.with_(S=a.seq_len, name=f"{lw.name}@S={a.seq_len}")
     T = a.seq_tile or lw.seq_tile
     S, Dm, V = lw.S, lw.Dm, lw.V
     h, w, t, g = (x.to(dev) for x in make_loss_inputs(lw, str(dev) if lw.gen_device == "cuda"

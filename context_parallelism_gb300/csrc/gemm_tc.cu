@@ -49,11 +49,21 @@ struct GLayout {
   static constexpr int kBytes = kAbort + 4 + 1024;
 };
 
-__device__ __forceinline__ void tile_coords(int t, int mt_n, int nt_n, int m_fastest, int& mt,
-                                            int& nt) {
+// Tile order. m_fastest: groups of group_m M tiles (all of them when group_m <= 0) are walked
+// M tile first, then N tile, group after group - the CTAs in flight then share a few B strips
+// and at most group_m A strips, which bounds the set of operand bytes that has to stay in L2.
+// Otherwise N tile first.
+__device__ __forceinline__ void tile_coords(int t, int mt_n, int nt_n, int m_fastest,
+                                            int group_m, int& mt, int& nt) {
   if (m_fastest) {
-    mt = t % mt_n;
-    nt = t / mt_n;
+    const int gm = (group_m > 0 && group_m < mt_n) ? group_m : mt_n;
+    const int per_group = gm * nt_n;
+    const int grp = t / per_group;
+    const int rem = t - grp * per_group;
+    const int m0 = grp * gm;
+    const int rows = min(gm, mt_n - m0);
+    mt = m0 + rem % rows;
+    nt = rem / rows;
   } else {
     nt = t % nt_n;
     mt = t / nt_n;
@@ -240,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
         int mt, nt;
-        tile_coords(t, mt_n, nt_n, a.m_fastest, mt, nt);
+        tile_coords(t, mt_n, nt_n, a.m_fastest, a.group_m, mt, nt);
         for (int kb = 0; kb < nk; ++kb) {
           if (!wait(empty + s, ph ^ 1)) {
             ok = false;
@@ -330,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int it = 0;
     for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
       int mt, nt;
-      tile_coords(t, mt_n, nt_n, a.m_fastest, mt, nt);
+      tile_coords(t, mt_n, nt_n, a.m_fastest, a.group_m, mt, nt);
       const int acc = it & 1;
       if (!wait(acc_full + acc, (it >> 1) & 1)) break;
       tc_fence_after();

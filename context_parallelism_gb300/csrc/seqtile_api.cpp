@@ -35,6 +35,13 @@ int lfail(int status, const char* fmt, ...) {
       return lfail(UPIPE_ERR_CUDA, "%s: %s", #call, cudaGetErrorString(e_));     \
   } while (0)
 
+// M tiles (128 tokens each) walked together by the two vocabulary GEMMs: the token rows of one
+// group (group x 128 x Dm x 2 bytes: 32 MiB at Dm 4096) stay in L2 while the vocabulary streams
+// past them once per group.
+#ifndef UPIPE_CE_GROUP_M
+#define UPIPE_CE_GROUP_M 32
+#endif
+
 constexpr size_t kAl = 256;
 inline size_t al(size_t x) { return (x + kAl - 1) / kAl * kAl; }
 
@@ -154,6 +161,7 @@ int upipe_ce_fwd(const void* h, const void* w, const int64_t* target, float* los
     a.N = static_cast<int>(V);
     a.K = Dm;
     a.m_fastest = 1;
+    a.group_m = UPIPE_CE_GROUP_M;
     a.target = target + r0;
     a.part = part;
     a.part_stride = p.T_pad;
@@ -205,6 +213,7 @@ int upipe_ce_bwd(const void* h, const void* w, const int64_t* target, const floa
     g.N = static_cast<int>(V);
     g.K = Dm;
     g.m_fastest = 1;
+    g.group_m = UPIPE_CE_GROUP_M;
     g.c = dl;
     g.ldc = V;
     g.target = target + r0;
