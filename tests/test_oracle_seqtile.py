@@ -154,3 +154,111 @@ def test_blocking_and_sampled_rows_agree_with_whole_problem():
     _, _, _, dw_full = ce_loss_bwd_ref(h, w, t, gs)
     _, _, _, dw_part = ce_rows_ref(h, w, t, gs, rows, vocab_rows=vr)
     assert np.allclose(dw_part, dw_full[vr], rtol=0, atol=1e-13)
+
+
+# ---- gated (SwiGLU) MLP ---------------------------------------------------------------------
+
+from oracle.seqtile_ref import mlp_bwd_ref, mlp_ref, mlp_rows_ref  # noqa: E402
+
+
+def _mlp_problem(rng, S, Dm, F):
+    x = rng.standard_normal((S, Dm))
+    w_gu = rng.standard_normal((2 * F, Dm)) * 0.6
+    w_d = rng.standard_normal((Dm, F)) * 0.6
+    dy = rng.standard_normal((S, Dm))
+    return x, w_gu, w_d, dy
+
+
+def test_mlp_finite_differences():
+    rng = np.random.default_rng(21)
+    S, Dm, F = 3, 4, 5
+    x, w_gu, w_d, dy = _mlp_problem(rng, S, Dm, F)
+    _, dx, dw_gu, dw_d = mlp_bwd_ref(x, w_gu, w_d, dy)
+
+    def f(xx, gg, dd):
+        return float(np.sum(dy * mlp_ref(xx, gg, dd)))
+
+    eps = 1e-6
+    for arr, grad, which in ((x, dx, 0), (w_gu, dw_gu, 1), (w_d, dw_d, 2)):
+        num = np.zeros_like(arr)
+        for idx in np.ndindex(*arr.shape):
+            p, m = arr.copy(), arr.copy()
+            p[idx] += eps
+            m[idx] -= eps
+            args_p = [x, w_gu, w_d]
+            args_m = [x, w_gu, w_d]
+            args_p[which], args_m[which] = p, m
+            num[idx] = (f(*args_p) - f(*args_m)) / (2 * eps)
+        assert np.abs(num - grad).max() <= 1e-6 * max(1.0, np.abs(grad).max()), which
+
+
+def test_mlp_matches_torch_autograd():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(23)
+    x, w_gu, w_d, dy = _mlp_problem(rng, 17, 12, 9)
+    y, dx, dw_gu, dw_d = mlp_bwd_ref(x, w_gu, w_d, dy, block=5)
+    X = torch.tensor(x, requires_grad=True)
+    G = torch.tensor(w_gu, requires_grad=True)
+    D = torch.tensor(w_d, requires_grad=True)
+    F = w_d.shape[1]
+    h = X @ G.T
+    Y = (torch.nn.functional.silu(h[:, :F]) * h[:, F:]) @ D.T
+    Y.backward(torch.tensor(dy))
+    assert np.allclose(y, Y.detach().numpy(), rtol=1e-12, atol=1e-12)
+    assert np.allclose(dx, X.grad.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.allclose(dw_gu, G.grad.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.allclose(dw_d, D.grad.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_mlp_closed_forms():
+    # gate weights zero: g = 0, silu(0) = 0, so y = 0; silu'(0) = 1/2, so dg = da*u/2, du = 0
+    rng = np.random.default_rng(25)
+    S, Dm, F = 6, 5, 4
+    x, w_gu, w_d, dy = _mlp_problem(rng, S, Dm, F)
+    w_gu[:F] = 0.0
+    y, dx, dw_gu, dw_d = mlp_bwd_ref(x, w_gu, w_d, dy)
+    assert np.all(y == 0.0) and np.all(dw_d == 0.0)
+    u = x @ w_gu[F:].T
+    da = dy @ w_d
+    assert np.allclose(dw_gu[:F], (0.5 * da * u).T @ x, rtol=0, atol=1e-12)
+    assert np.all(dw_gu[F:] == 0.0)
+    # huge positive gate: silu(g) -> g, so y -> ((x Wg^T) * (x Wu^T)) Wd^T
+    x2, w2, d2, _ = _mlp_problem(rng, 4, 3, 2)
+    w2[:2] = np.abs(w2[:2]) * 1e3
+    x2 = np.abs(x2)
+    g = x2 @ w2[:2].T
+    want = (g * (x2 @ w2[2:].T)) @ d2.T
+    assert np.allclose(mlp_ref(x2, w2, d2), want, rtol=1e-12, atol=0)
+
+
+def test_silu_matches_logistic_and_is_stable():
+    special = pytest.importorskip("scipy.special")
+    from oracle.seqtile_ref import _silu_parts
+    z = np.linspace(-800.0, 800.0, 4001)
+    s, ds = _silu_parts(z)
+    assert np.all(np.isfinite(s)) and np.all(np.isfinite(ds))
+    assert np.allclose(s, z * special.expit(z), rtol=1e-14, atol=1e-300)
+    h = 1e-6
+    zz = np.linspace(-20, 20, 81)
+    num = (_silu_parts(zz + h)[0] - _silu_parts(zz - h)[0]) / (2 * h)
+    assert np.allclose(_silu_parts(zz)[1], num, rtol=1e-7, atol=1e-9)
+
+
+def test_mlp_rows_and_blocking_agree_with_whole_problem():
+    rng = np.random.default_rng(27)
+    x, w_gu, w_d, dy = _mlp_problem(rng, 40, 6, 5)
+    a = mlp_bwd_ref(x, w_gu, w_d, dy, block=3)
+    b = mlp_bwd_ref(x, w_gu, w_d, dy, block=100)
+    for p, q in zip(a, b):
+        assert np.allclose(p, q, rtol=0, atol=1e-12)
+    rows = [0, 7, 39]
+    y, dx = mlp_rows_ref(x, w_gu, w_d, dy, rows)
+    assert np.allclose(y, b[0][rows], rtol=0, atol=1e-13)
+    assert np.allclose(dx, b[1][rows], rtol=0, atol=1e-13)
+    dys = np.zeros_like(dy)
+    dys[rows] = dy[rows]
+    _, _, dwg_full, dwd_full = mlp_bwd_ref(x, w_gu, w_d, dys)
+    gr, dr = [0, 3, 9], [1, 4]
+    _, _, dwg, dwd = mlp_rows_ref(x, w_gu, w_d, dys, rows, gu_rows=gr, d_rows=dr)
+    assert np.allclose(dwg, dwg_full[gr], rtol=0, atol=1e-12)
+    assert np.allclose(dwd, dwd_full[dr], rtol=0, atol=1e-12)
