@@ -14,7 +14,9 @@ GPU (the path does not shard on one box); value = total FLOPs of all ranks / max
 
 --workload llama8b_readout_s128k (or readout_small) measures the sequence-tiled readout +
 cross-entropy loss instead (one step = upipe_ce_fwd + upipe_ce_bwd over S tokens, seq_tile
-tokens at a time; FLOPs: fwd 2*S*V*Dm, bwd 3x that) and prints its own JSON line.
+tokens at a time; FLOPs: fwd 2*S*V*Dm, bwd 3x that) and prints its own JSON line;
+--workload llama8b_mlp_s128k (or mlp_small) the sequence-tiled SwiGLU MLP (upipe_mlp_fwd +
+upipe_mlp_bwd; FLOPs: fwd 6*S*Dm*F, bwd 16*S*Dm*F).
 """
 from __future__ import annotations
 
@@ -624,6 +626,7 @@ def run_sweep(a):
 
 
 LOSS_METRIC = "sequence-tiled readout + cross-entropy fwd+bwd TFLOP/s on 1 GB300"
+MLP_METRIC = "sequence-tiled SwiGLU MLP fwd+bwd TFLOP/s on 1 GB300"
 
 
 def loss_oracle_sample(lw, S_sample, inputs):
@@ -643,20 +646,9 @@ def loss_oracle_sample(lw, S_sample, inputs):
     return flops / dt / 1e12, dt, desc, cores
 
 
-def run_loss(a):
-    """The sequence-tiled loss on one GPU (N independent replicas under torchrun)."""
-    import torch
-    import torch.distributed as dist
-
-    import context_parallelism_gb300 as up
+def _loss_spec(a, dev, up):
     from workloads import LOSS_WORKLOADS, make_loss_inputs
-
-    rank, world, local = _dist()
-    if world > 1:
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
+    import torch
     lw = LOSS_WORKLOADS[a.workload]
     if a.seq_len:
         lw = lw.with_(S=a.seq_len, name=f"{lw.name}@S={a.seq_len}")
@@ -671,12 +663,69 @@ def run_loss(a):
     ws_bytes = up.upipe_ce_workspace_bytes(S, Dm, V, T, up.UPIPE_PASS_BOTH)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    return {
+        "metric": LOSS_METRIC, "name": lw.name, "seq_tile": T,
+        "fwd": lambda: up.upipe_ce_fwd(h, w, t, loss, lse, S, Dm, V, T, ws, ws_bytes, stream),
+        "bwd": lambda: up.upipe_ce_bwd(h, w, t, lse, g, dh, dw, S, Dm, V, T, ws, ws_bytes, stream),
+        "f_fwd": lw.flops_fwd(), "f_bwd": lw.flops_bwd(), "ws_bytes": ws_bytes,
+        "data": "synthetic (seeded: h N(0,1), w N(0,%g/sqrt(Dm)) bf16, uniform targets, "
+                "%.4f ignored)" % (lw.w_std, lw.ignore_frac),
+        "config": {"workload": lw.name, "S": S, "Dm": Dm, "V": V, "seq_tile": T,
+                   "l2": "inputs larger than L2 (w is %.2f GiB)" % (w.nbytes / 2**30)},
+        "extra": {"untiled_logits_gb": S * V * 4 / 1e9},
+        "inputs": (h, w, t, g), "outputs": (loss, lse, dh, dw),
+        "cpu": lambda: loss_oracle_sample(lw, min(S, 32), (h, w, t, g)),
+    }
 
-    def fwd():
-        up.upipe_ce_fwd(h, w, t, loss, lse, S, Dm, V, T, ws, ws_bytes, stream)
 
-    def bwd():
-        up.upipe_ce_bwd(h, w, t, lse, g, dh, dw, S, Dm, V, T, ws, ws_bytes, stream)
+def _mlp_spec(a, dev, up):
+    from workloads import MLP_WORKLOADS, make_mlp_inputs
+    import torch
+    mw = MLP_WORKLOADS[a.workload]
+    if a.seq_len:
+        mw = mw.with_(S=a.seq_len, name=f"{mw.name}@S={a.seq_len}")
+    T = a.seq_tile or mw.seq_tile
+    S, Dm, F = mw.S, mw.Dm, mw.F
+    x, w_gu, w_d, dy = (t.to(dev) for t in make_mlp_inputs(mw, str(dev) if mw.gen_device == "cuda"
+                                                         else "cpu"))
+    y = torch.empty_like(x)
+    dx = torch.empty_like(x)
+    dw_gu = torch.empty((2 * F, Dm), dtype=torch.float32, device=dev)
+    dw_d = torch.empty((Dm, F), dtype=torch.float32, device=dev)
+    ws_bytes = up.upipe_mlp_workspace_bytes(S, Dm, F, T, up.UPIPE_PASS_BOTH)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    return {
+        "metric": MLP_METRIC, "name": mw.name, "seq_tile": T,
+        "fwd": lambda: up.upipe_mlp_fwd(x, w_gu, w_d, y, S, Dm, F, T, ws, ws_bytes, stream),
+        "bwd": lambda: up.upipe_mlp_bwd(x, w_gu, w_d, dy, dx, dw_gu, dw_d, S, Dm, F, T, ws,
+                                        ws_bytes, stream),
+        "f_fwd": mw.flops_fwd(), "f_bwd": mw.flops_bwd(), "ws_bytes": ws_bytes,
+        "data": "synthetic (seeded: x, dy N(0,1), w_gu N(0,1/sqrt(Dm)), w_d N(0,1/sqrt(F)) bf16)",
+        "config": {"workload": mw.name, "S": S, "Dm": Dm, "F": F, "seq_tile": T,
+                   "l2": "inputs larger than L2 (x is %.2f GiB)" % (x.nbytes / 2**30)},
+        "extra": {"untiled_intermediates_gb": 5 * S * F * 2 / 1e9},
+        "inputs": (x, w_gu, w_d, dy), "outputs": (y, dx, dw_gu, dw_d),
+        "cpu": lambda: mlp_oracle_sample(mw, min(S, 256), (x, w_gu, w_d, dy)),
+    }
+
+
+def run_tiled(a, make_spec):
+    """A sequence-tiled workload (loss or MLP) on one GPU (N replicas under torchrun)."""
+    import torch
+    import torch.distributed as dist
+
+    import context_parallelism_gb300 as up
+
+    rank, world, local = _dist()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    sp = make_spec(a, dev, up)
+    fwd, bwd = sp["fwd"], sp["bwd"]
+    stream = torch.cuda.current_stream(dev)
 
     def barrier():
         if world > 1:
@@ -712,7 +761,7 @@ def run_loss(a):
     up.upipe_sync_status(stream)
     fwd_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
     bwd_ms = sum(e[1].elapsed_time(e[2]) for e in ev)
-    f_fwd, f_bwd = lw.flops_fwd(), lw.flops_bwd()
+    f_fwd, f_bwd = sp["f_fwd"], sp["f_bwd"]
     red = torch_reduce_max(dev) if world > 1 else None
     value, t_max = job_throughput(t0.elapsed_time(t1), a.steps, f_fwd + f_bwd, world, red)
     peaks, peak_src = _peaks()
@@ -723,39 +772,37 @@ def run_loss(a):
                 "unit": "TFLOP/s", "frac": achieved / peak if achieved else None,
                 "peak_source": f"{peak_src} bf16_tflops_sustained", "launches": gemm_n,
                 "avg_launch_ms": gemm_ms / max(gemm_n, 1),
-                "traffic": traffic_per_launch("loss_gemm", lw.name, T, None),
+                "traffic": traffic_per_launch("loss_gemm", sp["name"], sp["seq_tile"], None),
                 "traffic_unit": "bytes per launch"}
     kernels = {k: {"ms_per_step": tm / a.steps, "launches_per_step": n / a.steps}
                for k, (tm, n) in prof.items() if n}
+    config = dict(sp["config"])
+    config["parallelism"] = "replicas" if world > 1 else "single"
     line = {
-        "metric": LOSS_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "metric": sp["metric"], "value": value, "unit": UNIT, "n_gpus": world,
         "steps": a.steps, "warmup": a.warmup, "ms_per_step": t_max / a.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded: h N(0,1), w N(0,%g/sqrt(Dm)) bf16, uniform targets, "
-                "%.4f ignored)" % (lw.w_std, lw.ignore_frac),
-        "config": {"workload": lw.name, "S": S, "Dm": Dm, "V": V, "seq_tile": T,
-                   "l2": "inputs larger than L2 (w is %.2f GiB)" % (w.nbytes / 2**30),
-                   "parallelism": "replicas" if world > 1 else "single"},
+        "data": sp["data"], "config": config,
         "fwd_tflops": world * f_fwd * a.steps / (fwd_ms / 1e3) / 1e12,
         "bwd_tflops": world * f_bwd * a.steps / (bwd_ms / 1e3) / 1e12,
         "frac_of_bf16_peak": value / world / peak, "peak_tflops": peak,
-        "workspace_gb": ws_bytes / 1e9,
-        "untiled_logits_gb": S * V * 4 / 1e9,
+        "workspace_gb": sp["ws_bytes"] / 1e9, **sp["extra"],
         "roofline": roofline, "kernels": kernels, "gpu_launches": int(launches), "clocks": clk,
     }
     if not a.no_e2e:
-        # host buffers in (h, w, target, dloss), loss / lse / dh / dw out, every step
-        hh = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (h, w, t, g)]
-        for src, dst in zip((h, w, t, g), hh):
+        # host buffers in (every input), every output out, each step
+        ins, outs_d = sp["inputs"], sp["outputs"]
+        hh = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in ins]
+        for src, dst in zip(ins, hh):
             dst.copy_(src)
-        outs = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (loss, lse, dh, dw)]
+        outs = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in outs_d]
 
         def e2e_step():
-            for dst, src in zip((h, w, t, g), hh):
+            for dst, src in zip(ins, hh):
                 dst.copy_(src, non_blocking=True)
             fwd()
             bwd()
-            for dst, src in zip(outs, (loss, lse, dh, dw)):
+            for dst, src in zip(outs, outs_d):
                 dst.copy_(src, non_blocking=True)
 
         e2e_step()
@@ -769,11 +816,12 @@ def run_loss(a):
         line["e2e"] = {"value": e2e_value, "unit": UNIT,
                        "h2d_bytes_per_step": int(sum(x.nbytes for x in hh)),
                        "d2h_bytes_per_step": int(sum(x.nbytes for x in outs)),
-                       "method": "pinned host h, w, target, dloss copied in and loss, lse, dh, dw "
-                                 "copied out on the compute stream around upipe_ce_fwd/bwd"}
+                       "method": "every input copied in from pinned host memory and every "
+                                 "output copied out, on the compute stream, around the "
+                                 "forward and backward calls"}
         up.upipe_sync_status(stream)
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
-        tf, dt, desc, cores = loss_oracle_sample(lw, min(S, 32), (h, w, t, g))
+        tf, dt, desc, cores = sp["cpu"]()
         line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
                                 "sample": desc, "seconds": dt}
     if world > 1:
@@ -781,6 +829,50 @@ def run_loss(a):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def mlp_oracle_sample(mw, S_sample, inputs):
+    """Times the fp64 oracle's MLP forward + backward on the first S_sample tokens."""
+    import oracle
+    x, w_gu, w_d, dy = inputs
+    xs, dys = x[:S_sample].cpu(), dy[:S_sample].cpu()
+    flops = mw.with_(S=S_sample).flops_fwd() + mw.with_(S=S_sample).flops_bwd()
+    t0 = time.perf_counter()
+    oracle.mlp_bwd_ref(xs, w_gu.cpu(), w_d.cpu(), dys)
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    desc = (f"fp64 numpy oracle MLP fwd+bwd on the first {S_sample} of {mw.S} tokens, width "
+            f"{mw.Dm}, hidden {mw.F}; FLOPs by the same convention")
+    return flops / dt / 1e12, dt, desc, cores
+
+
+def run_mlp_reference(a):
+    """Reference arm for the MLP workloads: the fp64 oracle on the host cores, rank 0 only."""
+    rank, _, _ = _dist()
+    if rank != 0:
+        return
+    from workloads import MLP_WORKLOADS, make_mlp_inputs
+    mw = MLP_WORKLOADS[a.workload]
+    S_sample = min(mw.S, 256)
+    inputs = make_mlp_inputs(mw.with_(S=S_sample, gen_device="cpu"), "cpu")
+    vals = []
+    for i in range(a.warmup + a.steps):
+        tf, dt, desc, cores = mlp_oracle_sample(mw, S_sample, inputs)
+        if i >= a.warmup:
+            vals.append(dt)
+    flops = mw.with_(S=S_sample).flops_fwd() + mw.with_(S=S_sample).flops_bwd()
+    value = flops * len(vals) / sum(vals) / 1e12
+    print(json.dumps({
+        "impl": "reference", "metric": MLP_METRIC, "value": value, "unit": UNIT,
+        "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": 1000.0 * statistics.mean(vals), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": mw.name, "S": mw.S, "Dm": mw.Dm, "F": mw.F,
+                   "seq_tile": a.seq_tile or mw.seq_tile, "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc + " (recipe regenerated on the CPU at the sample length)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
 
 
 def run_loss_reference(a):
@@ -816,12 +908,18 @@ def run_loss_reference(a):
 
 def main():
     a = _args()
-    from workloads import LOSS_WORKLOADS
+    from workloads import LOSS_WORKLOADS, MLP_WORKLOADS
     if a.workload in LOSS_WORKLOADS:
         if a.impl == "reference":
             run_loss_reference(a)
         else:
-            run_loss(a)
+            run_tiled(a, _loss_spec)
+        return
+    if a.workload in MLP_WORKLOADS:
+        if a.impl == "reference":
+            run_mlp_reference(a)
+        else:
+            run_tiled(a, _mlp_spec)
         return
     if a.sweep:
         run_sweep(a)

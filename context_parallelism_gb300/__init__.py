@@ -61,6 +61,10 @@ SIGNATURES = {
     "upipe_ce_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i64, _i, _i64, _i64, _vp, _sz, _vp]),
     "upipe_ce_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i, _i64, _i64, _vp, _sz,
                           _vp]),
+    "upipe_mlp_workspace_bytes": (_sz, [_i64, _i, _i, _i64, _i]),
+    "upipe_mlp_fwd": (_i, [_vp, _vp, _vp, _vp, _i64, _i, _i, _i64, _vp, _sz, _vp]),
+    "upipe_mlp_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i, _i, _i64, _vp, _sz,
+                           _vp]),
 }
 
 
@@ -229,6 +233,27 @@ def upipe_ce_bwd(h, w, target, lse, dloss, dh, dw, S, Dm, V, seq_tile, workspace
     _check(st, "upipe_ce_bwd")
 
 
+def upipe_mlp_workspace_bytes(S, Dm, F, seq_tile, pass_=UPIPE_PASS_BOTH):
+    return int(_lib.upipe_mlp_workspace_bytes(S, Dm, F, seq_tile, pass_))
+
+
+def upipe_mlp_fwd(x, w_gu, w_d, y, S, Dm, F, seq_tile, workspace, workspace_bytes=None,
+                  stream=None):
+    wb = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    st = _lib.upipe_mlp_fwd(_ptr(x), _ptr(w_gu), _ptr(w_d), _ptr(y), S, Dm, F, seq_tile,
+                            _ptr(workspace), wb, _stream(stream, x, y, workspace))
+    _check(st, "upipe_mlp_fwd")
+
+
+def upipe_mlp_bwd(x, w_gu, w_d, dy, dx, dw_gu, dw_d, S, Dm, F, seq_tile, workspace,
+                  workspace_bytes=None, stream=None):
+    wb = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    st = _lib.upipe_mlp_bwd(_ptr(x), _ptr(w_gu), _ptr(w_d), _ptr(dy), _ptr(dx), _ptr(dw_gu),
+                            _ptr(dw_d), S, Dm, F, seq_tile, _ptr(workspace), wb,
+                            _stream(stream, x, dx, workspace))
+    _check(st, "upipe_mlp_bwd")
+
+
 # ---- convenience: allocate outputs / workspace with torch, then call the ABI -------------
 
 def _dims(q, k):
@@ -340,3 +365,38 @@ def ce_loss_backward(h, w, target, lse, dloss, seq_tile=8192, workspace=None, st
         workspace = torch.empty(need, dtype=torch.uint8, device=h.device)
     upipe_ce_bwd(h, w, target, lse, dloss, dh, dw, S, Dm, V, seq_tile, workspace, None, stream)
     return dh, dw
+
+
+def mlp_forward(x, w_gu, w_d, seq_tile=8192, workspace=None, stream=None):
+    """y = (silu(x Wg^T) * x Wu^T) Wd^T for x [S, Dm], w_gu = [Wg; Wu] [2F, Dm], w_d [Dm, F]
+    (bf16), seq_tile tokens at a time."""
+    import torch
+    S, Dm = x.shape
+    F = w_d.shape[1]
+    y = torch.empty((S, Dm), dtype=x.dtype, device=x.device)
+    need = upipe_mlp_workspace_bytes(S, Dm, F, seq_tile, UPIPE_PASS_FWD)
+    if need == 0:
+        upipe_mlp_fwd(x, w_gu, w_d, y, S, Dm, F, seq_tile, 0, 0, stream)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    upipe_mlp_fwd(x, w_gu, w_d, y, S, Dm, F, seq_tile, workspace, None, stream)
+    return y
+
+
+def mlp_backward(x, w_gu, w_d, dy, seq_tile=8192, workspace=None, stream=None):
+    """dx (bf16 [S, Dm]), dw_gu (float32 [2F, Dm]) and dw_d (float32 [Dm, F]) for the forward
+    above and the upstream gradient dy [S, Dm]."""
+    import torch
+    S, Dm = x.shape
+    F = w_d.shape[1]
+    dx = torch.empty_like(x)
+    dw_gu = torch.empty((2 * F, Dm), dtype=torch.float32, device=x.device)
+    dw_d = torch.empty((Dm, F), dtype=torch.float32, device=x.device)
+    need = upipe_mlp_workspace_bytes(S, Dm, F, seq_tile, UPIPE_PASS_BWD)
+    if need == 0:
+        upipe_mlp_bwd(x, w_gu, w_d, dy, dx, dw_gu, dw_d, S, Dm, F, seq_tile, 0, 0, stream)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    upipe_mlp_bwd(x, w_gu, w_d, dy, dx, dw_gu, dw_d, S, Dm, F, seq_tile, workspace, None,
+                  stream)
+    return dx, dw_gu, dw_d

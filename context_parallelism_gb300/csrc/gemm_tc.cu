@@ -23,6 +23,13 @@
 //   CE_BWD    logits -> dlogits = g_row * (exp(logit - lse_row) - [col == target]) as bf16
 //   STORE     C -> bf16
 //   ACC_F32   C -> fp32, added to what is there when accumulating, else stored
+// and those of the sequence-tiled gated MLP (same passages: "all the MLPs" are chunked):
+//   SWIGLU    gate and up projections in one tile: the B stage holds 128 rows of the gate
+//             block and the matching 128 rows of the up block (two TMA boxes), so one
+//             accumulator holds g (columns 0-127) and u (128-255) of the same 128 outputs;
+//             a = silu(g) * u -> bf16, and optionally g, u -> bf16 for the backward
+//   DSWIGLU   da = dy Wd -> dg = da * u * silu'(g), du = da * silu(g) -> bf16, reading the
+//             stored g, u
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -38,6 +45,11 @@ constexpr uint32_t kAStage = kBM * kBK * 2;  // 16 KiB
 constexpr uint32_t kBStage = kBN * kBK * 2;  // 32 KiB
 constexpr uint32_t kMnBox = 64 * kBK * 2;    // one 64-wide, 64-row MN-major box: 8 KiB
 constexpr float kLog2e = 1.4426950408889634f;
+
+// Output columns of one tile: the gated epilogue spends the 256 accumulator columns on 128
+// outputs (their gate and up halves).
+template <int EPI>
+constexpr int out_cols() { return EPI == kEpiSwiglu ? kBN / 2 : kBN; }
 
 struct GLayout {
   static constexpr int kA = 0;
@@ -155,6 +167,87 @@ struct Epi<kEpiStoreBf16> {
   __device__ void end(const GemmArgs&, int64_t, bool, int, int) {}
 };
 
+// silu(g) = g / (1 + e^-g) and silu'(g) = s (1 + g (1 - s)), s = 1 / (1 + e^-g); __expf and
+// __fdividef saturate cleanly at both ends (e^-g = inf gives silu = -0, s = 0).
+__device__ __forceinline__ void silu_parts(float g, float& sg, float& dsg) {
+  const float s = __fdividef(1.f, 1.f + __expf(-g));
+  sg = g * s;
+  dsg = s * fmaf(g, 1.f - s, 1.f);
+}
+
+template <>
+struct Epi<kEpiSwiglu> {
+  __device__ void begin(const GemmArgs&, int64_t, bool) {}
+  // g, u: the gate and up accumulators of output columns col0 .. col0+31
+  __device__ void slice2(const GemmArgs& a, int64_t row, bool row_ok, int col0, const float* g,
+                         const float* u) {
+    float o[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float s = __fdividef(1.f, 1.f + __expf(-g[j]));
+      o[j] = g[j] * s * u[j];
+    }
+    if (!row_ok) return;
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.c) + row * a.ldc + col0);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) dst[v] = pack8(o + 8 * v);
+    if (a.c2) {
+      __nv_bfloat16* base = static_cast<__nv_bfloat16*>(a.c2) + row * a.ldc2;
+      uint4* dg = reinterpret_cast<uint4*>(base + col0);
+      uint4* du = reinterpret_cast<uint4*>(base + a.split + col0);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        dg[v] = pack8(g + 8 * v);
+        du[v] = pack8(u + 8 * v);
+      }
+    }
+  }
+  __device__ void end(const GemmArgs&, int64_t, bool, int, int) {}
+};
+
+__device__ __forceinline__ void unpack8(uint4 v, float* x) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+template <>
+struct Epi<kEpiDSwiglu> {
+  __device__ void begin(const GemmArgs&, int64_t, bool) {}
+  __device__ void slice(const GemmArgs& a, int64_t row, bool row_ok, int col0, const float* da) {
+    if (!row_ok) return;
+    const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(a.aux) + row * a.ld_aux;
+    const uint4* pg = reinterpret_cast<const uint4*>(src + col0);
+    const uint4* pu = reinterpret_cast<const uint4*>(src + a.split + col0);
+    float dg[32], du[32];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      float g[8], u[8];
+      unpack8(pg[v], g);
+      unpack8(pu[v], u);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float sg, dsg;
+        silu_parts(g[i], sg, dsg);
+        dg[8 * v + i] = da[8 * v + i] * u[i] * dsg;
+        du[8 * v + i] = da[8 * v + i] * sg;
+      }
+    }
+    __nv_bfloat16* base = static_cast<__nv_bfloat16*>(a.c) + row * a.ldc;
+    uint4* og = reinterpret_cast<uint4*>(base + col0);
+    uint4* ou = reinterpret_cast<uint4*>(base + a.split + col0);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      og[v] = pack8(dg + 8 * v);
+      ou[v] = pack8(du + 8 * v);
+    }
+  }
+  __device__ void end(const GemmArgs&, int64_t, bool, int, int) {}
+};
+
 template <>
 struct Epi<kEpiAccF32> {
   __device__ void begin(const GemmArgs&, int64_t, bool) {}
@@ -197,7 +290,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int mt_n = (a.M + kBM - 1) / kBM;
-  const int nt_n = (a.N + kBN - 1) / kBN;
+  constexpr int kOut = out_cols<EPI>();
+  const int nt_n = (a.N + kOut - 1) / kOut;
   const int nk = (a.K + kBK - 1) / kBK;
   const int n_tiles = mt_n * nt_n;
 
@@ -266,7 +360,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             tma_load_3d(sa, &tm_a, kb * kBK, mt * kBM, 0, full + s);
           }
-          if (B_MN) {
+          if (EPI == kEpiSwiglu) {
+            // 128 gate rows, then the 128 up rows of the same outputs (128-row boxes)
+            tma_load_3d(sb, &tm_b, kb * kBK, nt * kOut, 0, full + s);
+            tma_load_3d(sb + kBStage / 2, &tm_b, kb * kBK, a.split + nt * kOut, 0, full + s);
+          } else if (B_MN) {
 #pragma unroll
             for (int i = 0; i < kBN / 64; ++i)
               tma_load_3d(sb + i * kMnBox, &tm_b, nt * kBN + 64 * i, kb * kBK, 0, full + s);
@@ -346,16 +444,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int64_t row = static_cast<int64_t>(mt) * kBM + r_in;
       const bool row_ok = row < a.M;
-      const int n0 = nt * kBN;
+      const int n0 = nt * kOut;
       const uint32_t tD = tmem + (static_cast<uint32_t>(32 * quarter) << 16) +
                           static_cast<uint32_t>(acc * kBN);
       Epi<EPI> e;
       e.begin(a, row, row_ok);
-      for (int c = 0; c < kBN; c += 32) {
-        if (n0 + c >= a.N) break;  // N % 64 == 0: a slice is wholly inside or outside
-        uint32_t r[32];
-        tmem_ld32_sync(tD + static_cast<uint32_t>(c), r);
-        e.slice(a, row, row_ok, n0 + c, reinterpret_cast<const float*>(r));
+      if constexpr (EPI == kEpiSwiglu) {
+        for (int c = 0; c < kOut; c += 32) {  // N % 128 == 0: every slice is inside
+          uint32_t rg[32], ru[32];
+          tmem_ld32_sync(tD + static_cast<uint32_t>(c), rg);
+          tmem_ld32_sync(tD + static_cast<uint32_t>(kOut + c), ru);
+          e.slice2(a, row, row_ok, n0 + c, reinterpret_cast<const float*>(rg),
+                   reinterpret_cast<const float*>(ru));
+        }
+      } else {
+        for (int c = 0; c < kBN; c += 32) {
+          if (n0 + c >= a.N) break;  // N % 64 == 0: a slice is wholly inside or outside
+          uint32_t r[32];
+          tmem_ld32_sync(tD + static_cast<uint32_t>(c), r);
+          e.slice(a, row, row_ok, n0 + c, reinterpret_cast<const float*>(r));
+        }
       }
       e.end(a, row, row_ok, nt, n0);
       tc_fence_before();
@@ -405,7 +513,8 @@ cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const GemmA
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const int64_t tiles = static_cast<int64_t>((a.M + kBM - 1) / kBM) * ((a.N + kBN - 1) / kBN);
+  constexpr int kOut = out_cols<EPI>();
+  const int64_t tiles = static_cast<int64_t>((a.M + kBM - 1) / kBM) * ((a.N + kOut - 1) / kOut);
   const int grid = static_cast<int>(tiles < grid_cap ? tiles : grid_cap);
   if (grid <= 0) return cudaSuccess;
   launch_begin(6, stream);
@@ -424,6 +533,9 @@ cudaError_t launch_gemm_tc(int epi, bool a_mn, bool b_mn, const CUtensorMap& ta,
   if (epi == kEpiCeBwd && !a_mn && !b_mn) return launch_one<kEpiCeBwd, false, false>(ta, tb, a, grid_cap, stream);
   if (epi == kEpiStoreBf16 && !a_mn && b_mn) return launch_one<kEpiStoreBf16, false, true>(ta, tb, a, grid_cap, stream);
   if (epi == kEpiAccF32 && a_mn && b_mn) return launch_one<kEpiAccF32, true, true>(ta, tb, a, grid_cap, stream);
+  if (epi == kEpiStoreBf16 && !a_mn && !b_mn) return launch_one<kEpiStoreBf16, false, false>(ta, tb, a, grid_cap, stream);
+  if (epi == kEpiSwiglu && !a_mn && !b_mn) return launch_one<kEpiSwiglu, false, false>(ta, tb, a, grid_cap, stream);
+  if (epi == kEpiDSwiglu && !a_mn && b_mn) return launch_one<kEpiDSwiglu, false, true>(ta, tb, a, grid_cap, stream);
   return cudaErrorInvalidValue;
 }
 

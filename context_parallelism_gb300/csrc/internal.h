@@ -111,7 +111,14 @@ cudaError_t launch_dq_convert(const float* dqacc, void* dq, int B, int64_t S, in
 
 // ---- sequence-tiled loss (gemm_tc.cu) ------------------------------------------------------
 // C[m, n] = sum_k A(m, k) B(n, k) over 128 x 256 tiles, with the epilogue chosen by `epi`.
-enum : int { kEpiCeFwd = 0, kEpiCeBwd = 1, kEpiStoreBf16 = 2, kEpiAccF32 = 3 };
+enum : int {
+  kEpiCeFwd = 0,
+  kEpiCeBwd = 1,
+  kEpiStoreBf16 = 2,
+  kEpiAccF32 = 3,
+  kEpiSwiglu = 4,   // N = F outputs per row; B = w_gu [2F][K] with the up block at row `split`
+  kEpiDSwiglu = 5,  // c = dgu [M][2F]: dg at column j, du at split + j; aux = gu likewise
+};
 
 struct GemmArgs {
   int M, N, K;            // N % 64 == 0; M, K any (tensor maps zero-fill past the edges)
@@ -126,12 +133,18 @@ struct GemmArgs {
   float* part;            // CE_FWD: float2 [ceil(N/256)][part_stride] (max in log2 units, sum)
   int64_t part_stride;
   float* tlogit;          // CE_FWD: [M] logit at the target
+  void* c2;               // SWIGLU: optional bf16 g | u store [M][ldc2] (u at column split + j)
+  int64_t ldc2;
+  const void* aux;        // DSWIGLU: bf16 g | u [M][ld_aux]
+  int64_t ld_aux;
+  int split;              // SWIGLU / DSWIGLU: F, the offset of the up half
   uint32_t* err;
 };
 
 // Supported (epi, A MN-major, B MN-major): (CE_FWD, 0, 0), (CE_BWD, 0, 0), (STORE, 0, 1),
-// (ACC_F32, 1, 1). K-major maps have 128-row (A) / 256-row (B) boxes; MN-major maps 64-row
-// boxes; all 64 columns wide with 128-byte swizzle. The grid is min(tiles, grid_cap) CTAs.
+// (STORE, 0, 0), (ACC_F32, 1, 1), (SWIGLU, 0, 0), (DSWIGLU, 0, 1). K-major maps have 128-row
+// (A) / 256-row (B; 128-row for SWIGLU, loaded twice) boxes; MN-major maps 64-row boxes; all
+// 64 columns wide with 128-byte swizzle. The grid is min(tiles, grid_cap) CTAs.
 cudaError_t launch_gemm_tc(int epi, bool a_mn, bool b_mn, const CUtensorMap& ta,
                            const CUtensorMap& tb, const GemmArgs& a, int grid_cap,
                            cudaStream_t stream);

@@ -1,5 +1,5 @@
-// C ABI of the sequence-tiled readout + cross-entropy loss: validation, workspace plan and
-// the per-tile launch sequence.
+// C ABI of the sequence-tiled per-token computations - the readout + cross-entropy loss and the
+// gated (SwiGLU) MLP: validation, workspace plans and the per-tile launch sequences.
 //
 // Sequence tiling chunks the per-token computations along the sequence so that no buffer has
 // the whole sequence along one dimension ("Road to 5 million sequence length" talk notes,
@@ -9,6 +9,11 @@
 //             vocabulary tile, the target's logit), then one merge launch -> loss, lse;
 //   backward: logits GEMM again with the CE_BWD epilogue -> dlogits (bf16, seq_tile x V, the
 //             only large buffer), dh_tile = dlogits w (stored), dw += dlogits^T h_tile.
+// and for the MLP (y = (silu(x Wg^T) * x Wu^T) Wd^T), per tile:
+//   forward:  gate/up GEMM with the SWIGLU epilogue -> a (bf16, seq_tile x F), y = a Wd^T;
+//   backward: the gate/up GEMM again (a, and g | u for the gating derivative), da = dy Wd with
+//             the DSWIGLU epilogue -> dg | du, dWd += dy^T a, dWgu += (dg | du)^T x,
+//             dx = (dg | du) [Wg; Wu].
 #include <cstdarg>
 #include <cstdio>
 
@@ -242,6 +247,214 @@ int upipe_ce_bwd(const void* h, const void* w, const int64_t* target, const floa
     y.accumulate = r0 > 0 ? 1 : 0;
     y.err = err;
     LOSS_CUDA(launch_gemm_tc(kEpiAccF32, true, true, tdl_mn, th_mn, y, cap, stream));
+  }
+  return UPIPE_OK;
+}
+
+}  // extern "C"
+
+// ---- sequence-tiled gated MLP -------------------------------------------------------------
+
+namespace upipe {
+namespace {
+
+struct MlpPlan {
+  int64_t T = 0;
+  size_t a = 0, gu = 0, dgu = 0, f_total = 0, b_total = 0;
+};
+
+int check_mlp_shape(int64_t S, int Dm, int F, int64_t seq_tile) {
+  if (S < 1 || Dm < 1 || F < 1 || seq_tile < 1)
+    return lfail(UPIPE_ERR_INVALID_ARG, "S, Dm, F, seq_tile must be positive");
+  if (Dm % 64 != 0 || F % 128 != 0 || seq_tile % 128 != 0)
+    return lfail(UPIPE_ERR_UNSUPPORTED, "need Dm %% 64 == 0, F %% 128 == 0, seq_tile %% 128 == 0");
+  if (2 * static_cast<int64_t>(F) >= (int64_t(1) << 31))
+    return lfail(UPIPE_ERR_UNSUPPORTED, "2F must be below 2^31");
+  return UPIPE_OK;
+}
+
+MlpPlan make_mlp_plan(int64_t S, int F, int64_t seq_tile) {
+  MlpPlan p;
+  p.T = seq_tile < S ? seq_tile : S;
+  const size_t tf = static_cast<size_t>(p.T) * F * 2;  // one [T][F] bf16 buffer
+  p.a = 0;
+  p.gu = al(tf);
+  p.dgu = p.gu + al(2 * tf);
+  p.f_total = al(tf);
+  p.b_total = p.dgu + al(2 * tf);
+  return p;
+}
+
+}  // namespace
+}  // namespace upipe
+
+extern "C" {
+
+size_t upipe_mlp_workspace_bytes(int64_t S, int Dm, int F, int64_t seq_tile, int pass) {
+  if (check_mlp_shape(S, Dm, F, seq_tile) != UPIPE_OK) return 0;
+  if (pass < UPIPE_PASS_FWD || pass > UPIPE_PASS_BOTH) return 0;
+  const MlpPlan p = make_mlp_plan(S, F, seq_tile);
+  if (pass == UPIPE_PASS_FWD) return p.f_total;
+  return p.b_total;  // the backward's buffers include the forward's
+}
+
+int upipe_mlp_fwd(const void* x, const void* w_gu, const void* w_d, void* y, int64_t S, int Dm,
+                  int F, int64_t seq_tile, void* workspace, size_t workspace_bytes,
+                  void* stream_) {
+  set_last_error("");
+  int st = check_mlp_shape(S, Dm, F, seq_tile);
+  if (st != UPIPE_OK) return st;
+  const void* ptrs[5] = {x, w_gu, w_d, y, workspace};
+  const char* names[5] = {"x", "w_gu", "w_d", "y", "workspace"};
+  int dev = -1;
+  st = check_device_ptrs(ptrs, names, 5, &dev);
+  if (st != UPIPE_OK) return st;
+  const MlpPlan p = make_mlp_plan(S, F, seq_tile);
+  if (workspace_bytes < p.f_total)
+    return lfail(UPIPE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes,
+                 p.f_total);
+  LOSS_CUDA(cudaSetDevice(dev));
+  uint32_t* err = nullptr;
+  st = device_status_word(dev, &err);
+  if (st != UPIPE_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  void* a_ws = static_cast<uint8_t*>(workspace) + p.a;
+  const int cap = sm_count(dev);
+
+  CUtensorMap t_wgu, t_wd, t_x, t_a;
+  LOSS_CUDA(make_tmap_bf16(&t_wgu, w_gu, Dm, 2 * static_cast<int64_t>(F), 1, 128));
+  LOSS_CUDA(make_tmap_bf16(&t_wd, w_d, F, Dm, 1, 256));  // Wd as B [N = Dm][K = F]
+  for (int64_t r0 = 0; r0 < S; r0 += p.T) {
+    const int64_t Mc = (S - r0) < p.T ? (S - r0) : p.T;
+    LOSS_CUDA(make_tmap_bf16(&t_x, bf16_rows(x, r0, Dm), Dm, Mc, 1, 128));
+    LOSS_CUDA(make_tmap_bf16(&t_a, a_ws, F, Mc, 1, 128));
+    GemmArgs g{};
+    g.M = static_cast<int>(Mc);
+    g.N = F;
+    g.K = Dm;
+    g.m_fastest = 1;
+    g.group_m = UPIPE_CE_GROUP_M;
+    g.c = a_ws;
+    g.ldc = F;
+    g.split = F;
+    g.err = err;
+    LOSS_CUDA(launch_gemm_tc(kEpiSwiglu, false, false, t_x, t_wgu, g, cap, stream));
+    GemmArgs o{};
+    o.M = static_cast<int>(Mc);
+    o.N = Dm;
+    o.K = F;
+    o.m_fastest = 0;
+    o.c = static_cast<uint8_t*>(y) + r0 * Dm * 2;
+    o.ldc = Dm;
+    o.err = err;
+    LOSS_CUDA(launch_gemm_tc(kEpiStoreBf16, false, false, t_a, t_wd, o, cap, stream));
+  }
+  return UPIPE_OK;
+}
+
+int upipe_mlp_bwd(const void* x, const void* w_gu, const void* w_d, const void* dy, void* dx,
+                  float* dw_gu, float* dw_d, int64_t S, int Dm, int F, int64_t seq_tile,
+                  void* workspace, size_t workspace_bytes, void* stream_) {
+  set_last_error("");
+  int st = check_mlp_shape(S, Dm, F, seq_tile);
+  if (st != UPIPE_OK) return st;
+  const void* ptrs[8] = {x, w_gu, w_d, dy, dx, dw_gu, dw_d, workspace};
+  const char* names[8] = {"x", "w_gu", "w_d", "dy", "dx", "dw_gu", "dw_d", "workspace"};
+  int dev = -1;
+  st = check_device_ptrs(ptrs, names, 8, &dev);
+  if (st != UPIPE_OK) return st;
+  const MlpPlan p = make_mlp_plan(S, F, seq_tile);
+  if (workspace_bytes < p.b_total)
+    return lfail(UPIPE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes,
+                 p.b_total);
+  LOSS_CUDA(cudaSetDevice(dev));
+  uint32_t* err = nullptr;
+  st = device_status_word(dev, &err);
+  if (st != UPIPE_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* a_ws = ws + p.a;
+  void* gu_ws = ws + p.gu;
+  void* dgu_ws = ws + p.dgu;
+  const int64_t F2 = 2 * static_cast<int64_t>(F);
+  const int cap = sm_count(dev);
+
+  CUtensorMap t_wgu_k, t_wgu_mn, t_wd_mn, t_x_k, t_x_mn, t_dy_k, t_dy_mn, t_a_mn, t_dgu_k,
+      t_dgu_mn;
+  LOSS_CUDA(make_tmap_bf16(&t_wgu_k, w_gu, Dm, F2, 1, 128));  // [Wg; Wu] as B [N][K = Dm]
+  LOSS_CUDA(make_tmap_bf16(&t_wgu_mn, w_gu, Dm, F2, 1, 64));  // as B [K = 2F][N = Dm]
+  LOSS_CUDA(make_tmap_bf16(&t_wd_mn, w_d, F, Dm, 1, 64));     // Wd as B [K = Dm][N = F]
+  for (int64_t r0 = 0; r0 < S; r0 += p.T) {
+    const int64_t Mc = (S - r0) < p.T ? (S - r0) : p.T;
+    const uint8_t* xt = bf16_rows(x, r0, Dm);
+    const uint8_t* dyt = bf16_rows(dy, r0, Dm);
+    LOSS_CUDA(make_tmap_bf16(&t_x_k, xt, Dm, Mc, 1, 128));
+    LOSS_CUDA(make_tmap_bf16(&t_x_mn, xt, Dm, Mc, 1, 64));
+    LOSS_CUDA(make_tmap_bf16(&t_dy_k, dyt, Dm, Mc, 1, 128));
+    LOSS_CUDA(make_tmap_bf16(&t_dy_mn, dyt, Dm, Mc, 1, 64));
+    LOSS_CUDA(make_tmap_bf16(&t_a_mn, a_ws, F, Mc, 1, 64));
+    LOSS_CUDA(make_tmap_bf16(&t_dgu_k, dgu_ws, F2, Mc, 1, 128));
+    LOSS_CUDA(make_tmap_bf16(&t_dgu_mn, dgu_ws, F2, Mc, 1, 64));
+
+    GemmArgs r{};  // recompute: a, and g | u
+    r.M = static_cast<int>(Mc);
+    r.N = F;
+    r.K = Dm;
+    r.m_fastest = 1;
+    r.group_m = UPIPE_CE_GROUP_M;
+    r.c = a_ws;
+    r.ldc = F;
+    r.c2 = gu_ws;
+    r.ldc2 = F2;
+    r.split = F;
+    r.err = err;
+    LOSS_CUDA(launch_gemm_tc(kEpiSwiglu, false, false, t_x_k, t_wgu_k, r, cap, stream));
+
+    GemmArgs d{};  // da = dy Wd -> dg | du
+    d.M = static_cast<int>(Mc);
+    d.N = F;
+    d.K = Dm;
+    d.m_fastest = 1;
+    d.group_m = UPIPE_CE_GROUP_M;
+    d.c = dgu_ws;
+    d.ldc = F2;
+    d.aux = gu_ws;
+    d.ld_aux = F2;
+    d.split = F;
+    d.err = err;
+    LOSS_CUDA(launch_gemm_tc(kEpiDSwiglu, false, true, t_dy_k, t_wd_mn, d, cap, stream));
+
+    GemmArgs wd{};  // dWd += dy^T a
+    wd.M = Dm;
+    wd.N = F;
+    wd.K = static_cast<int>(Mc);
+    wd.m_fastest = 0;
+    wd.c = dw_d;
+    wd.ldc = F;
+    wd.accumulate = r0 > 0 ? 1 : 0;
+    wd.err = err;
+    LOSS_CUDA(launch_gemm_tc(kEpiAccF32, true, true, t_dy_mn, t_a_mn, wd, cap, stream));
+
+    GemmArgs wg{};  // dWgu += (dg | du)^T x
+    wg.M = static_cast<int>(F2);
+    wg.N = Dm;
+    wg.K = static_cast<int>(Mc);
+    wg.m_fastest = 0;
+    wg.c = dw_gu;
+    wg.ldc = Dm;
+    wg.accumulate = r0 > 0 ? 1 : 0;
+    wg.err = err;
+    LOSS_CUDA(launch_gemm_tc(kEpiAccF32, true, true, t_dgu_mn, t_x_mn, wg, cap, stream));
+
+    GemmArgs gx{};  // dx = (dg | du) [Wg; Wu]
+    gx.M = static_cast<int>(Mc);
+    gx.N = Dm;
+    gx.K = static_cast<int>(F2);
+    gx.m_fastest = 0;
+    gx.c = static_cast<uint8_t*>(dx) + r0 * Dm * 2;
+    gx.ldc = Dm;
+    gx.err = err;
+    LOSS_CUDA(launch_gemm_tc(kEpiStoreBf16, false, true, t_dgu_k, t_wgu_mn, gx, cap, stream));
   }
   return UPIPE_OK;
 }

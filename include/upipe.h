@@ -216,6 +216,33 @@ int upipe_ce_bwd(const void* h, const void* w, const int64_t* target, const floa
                  const float* dloss, void* dh, float* dw, int64_t S, int Dm, int64_t V,
                  int64_t seq_tile, void* workspace, size_t workspace_bytes, void* stream);
 
+/* ---- Sequence tiling: gated (SwiGLU) MLP ------------------------------------------------
+ *
+ * The MLP is the other per-token computation the same passages chunk along the sequence.
+ * Computed seq_tile tokens at a time, so the [S][F] intermediates never exist; each tile's
+ * intermediates are recomputed in the backward rather than kept. Definition (no biases;
+ * silu(z) = z / (1 + e^-z)):
+ *   g = x Wg^T, u = x Wu^T, a = silu(g) * u, y = a Wd^T;
+ *   backward, for dy: da = dy Wd, dg = da * u * silu'(g), du = da * silu(g),
+ *   dx = dg Wg + du Wu, dWd = dy^T a, dWg = dg^T x, dWu = du^T x.
+ * Layouts (dense row-major, bf16 unless noted): x, y, dy, dx [S][Dm]; w_gu [2F][Dm] = Wg
+ * (rows 0..F-1) stacked on Wu (rows F..2F-1); w_d [Dm][F]; dw_gu float32 [2F][Dm] and dw_d
+ * float32 [Dm][F], both overwritten with the sum over all tokens. Every pointer: device
+ * memory of one device, 16-byte aligned. UPIPE_ERR_UNSUPPORTED unless Dm % 64 == 0,
+ * F % 128 == 0 and seq_tile % 128 == 0; S >= 1 (ragged last tile). All six GEMMs of a tile
+ * run on the tensor cores (bf16 operands, fp32 accumulation); a, g, u, dg, du are rounded to
+ * bf16 between GEMMs. Workspace (upipe_mlp_workspace_bytes): forward T*F*2 bytes (a),
+ * backward 5*T*F*2 (a, g|u, dg|du), T = min(seq_tile, S), each buffer rounded up to 256;
+ * pass BOTH is the backward's.
+ */
+size_t upipe_mlp_workspace_bytes(int64_t S, int Dm, int F, int64_t seq_tile, int pass);
+int upipe_mlp_fwd(const void* x, const void* w_gu, const void* w_d, void* y, int64_t S, int Dm,
+                  int F, int64_t seq_tile, void* workspace, size_t workspace_bytes,
+                  void* stream);
+int upipe_mlp_bwd(const void* x, const void* w_gu, const void* w_d, const void* dy, void* dx,
+                  float* dw_gu, float* dw_d, int64_t S, int Dm, int F, int64_t seq_tile,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
 /* ---- Diagnostics ---------------------------------------------------------------------- */
 
 /* Kernel classes for launch counting and profiling. */
@@ -226,7 +253,7 @@ enum {
   UPIPE_K_ATTN_BWD = 3,   /* backward attention kernel */
   UPIPE_K_DQ_CONVERT = 4, /* dq float32 -> bf16 token-major */
   UPIPE_K_OTHER = 5,      /* self-tests */
-  UPIPE_K_LOSS_GEMM = 6,  /* sequence-tiled loss: tensor-core GEMMs with their epilogues */
+  UPIPE_K_LOSS_GEMM = 6,  /* sequence-tiled loss and MLP: tensor-core GEMMs + epilogues */
   UPIPE_K_LOSS_MERGE = 7, /* sequence-tiled loss: per-token merge of the vocabulary tiles */
   UPIPE_K_COUNT = 8
 };

@@ -216,3 +216,35 @@ def test_loss_calls_validate_before_device_access():
     assert st == up.UPIPE_ERR_INVALID_ARG
     assert "NULL" in up.upipe_last_error_message()
     assert lib is not None
+
+
+# ---- sequence-tiled gated MLP ---------------------------------------------------------------
+
+@pytest.mark.parametrize("S,Dm,F,T", [(131072, 4096, 14336, 8192), (1000, 256, 384, 256),
+                                      (1, 64, 128, 128)])
+def test_mlp_workspace_matches_formula(S, Dm, F, T):
+    al = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    Tt = min(T, S)
+    tf = Tt * F * 2
+    assert up.upipe_mlp_workspace_bytes(S, Dm, F, T, up.UPIPE_PASS_FWD) == al(tf)
+    bwd = al(tf) + 2 * al(2 * tf)
+    assert up.upipe_mlp_workspace_bytes(S, Dm, F, T, up.UPIPE_PASS_BWD) == bwd
+    assert up.upipe_mlp_workspace_bytes(S, Dm, F, T, up.UPIPE_PASS_BOTH) == bwd
+    # bounded by the tile: the same at 32x the sequence
+    S1 = max(S, T)
+    assert up.upipe_mlp_workspace_bytes(32 * S1, Dm, F, T, up.UPIPE_PASS_BWD) == \
+        up.upipe_mlp_workspace_bytes(S1, Dm, F, T, up.UPIPE_PASS_BWD)
+
+
+@pytest.mark.parametrize("S,Dm,F,T", [(0, 64, 128, 128), (128, 96, 128, 128),
+                                      (128, 64, 192, 128), (128, 64, 128, 64)])
+def test_mlp_workspace_zero_for_invalid(S, Dm, F, T):
+    assert up.upipe_mlp_workspace_bytes(S, Dm, F, T, up.UPIPE_PASS_BOTH) == 0
+
+
+def test_mlp_calls_validate_before_device_access():
+    st = up._lib.upipe_mlp_fwd(None, None, None, None, 128, 64, 128, 128, None, 0, None)
+    assert st == up.UPIPE_ERR_INVALID_ARG
+    st = up._lib.upipe_mlp_bwd(None, None, None, None, None, None, None, 128, 64, 192, 128,
+                               None, 0, None)
+    assert st == up.UPIPE_ERR_UNSUPPORTED

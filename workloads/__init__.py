@@ -211,3 +211,53 @@ def make_loss_inputs(lw: LossWorkload, device: str | None = None):
     n = int((target >= 0).sum().item())
     dloss = torch.full((lw.S,), 1.0 / max(1, n), dtype=torch.float32, device=dev)
     return h, w, target, dloss
+
+
+# ---- sequence-tiled gated MLP ---------------------------------------------------------------
+
+@dataclass(frozen=True)
+class MlpWorkload:
+    """A gated (SwiGLU) MLP over S tokens.
+
+    Recipe: from ONE ``torch.Generator`` seeded with ``seed``, in this order, each drawn as
+    fp32 normals and rounded to bf16: x [S, Dm] with std 1 (a normalised hidden state),
+    w_gu [2F, Dm] (gate rows, then up rows) with std 1/sqrt(Dm), w_d [Dm, F] with std
+    1/sqrt(F), and the upstream gradient dy [S, Dm] with std 1. Shapes stand in for a
+    Llama3-8B-shaped MLP (Dm 4096, F 14336); no weights are involved."""
+    name: str
+    S: int
+    Dm: int
+    F: int
+    seq_tile: int
+    seed: int
+    gen_device: str = "cpu"
+
+    def flops_fwd(self) -> float:
+        """Gate/up projection 4 S Dm F plus down projection 2 S Dm F."""
+        return 6.0 * self.S * self.Dm * self.F
+
+    def flops_bwd(self) -> float:
+        """Gate/up recompute 4, da 2, dWd 2, dWgu 4, dx 4 (units of S Dm F)."""
+        return 16.0 * self.S * self.Dm * self.F
+
+    def with_(self, **kw) -> "MlpWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+MLP_WORKLOADS = {
+    "mlp_small": MlpWorkload("mlp_small", S=1000, Dm=256, F=384, seq_tile=256, seed=30),
+    "llama8b_mlp_s128k": MlpWorkload("llama8b_mlp_s128k", S=131072, Dm=4096, F=14336,
+                                     seq_tile=8192, seed=31, gen_device="cuda"),
+}
+
+
+def make_mlp_inputs(mw: MlpWorkload, device: str | None = None):
+    """Return (x, w_gu, w_d, dy), all bf16."""
+    dev = device or mw.gen_device
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(mw.seed)
+    x = _normal_bf16((mw.S, mw.Dm), gen, dev, 1.0)
+    w_gu = _normal_bf16((2 * mw.F, mw.Dm), gen, dev, 1.0 / math.sqrt(mw.Dm))
+    w_d = _normal_bf16((mw.Dm, mw.F), gen, dev, 1.0 / math.sqrt(mw.F))
+    dy = _normal_bf16((mw.S, mw.Dm), gen, dev, 1.0)
+    return x, w_gu, w_d, dy
