@@ -428,7 +428,10 @@ int upipe_mlp_bwd(const void* x, const void* w_gu, const void* w_d, const void* 
     wd.M = Dm;
     wd.N = F;
     wd.K = static_cast<int>(Mc);
-    wd.m_fastest = 0;
+    // M tiles first, 16 at a time: the CTAs in flight share 16 dy strips (32 MiB at 8192
+    // tokens) and stream each strip of a about twice per tile, instead of all of a per wave
+    wd.m_fastest = 1;
+    wd.group_m = 16;
     wd.c = dw_d;
     wd.ldc = F;
     wd.accumulate = r0 > 0 ? 1 : 0;
