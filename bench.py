@@ -80,14 +80,23 @@ TRAFFIC = {
                  "files": ["context_parallelism_gb300/csrc/attn_fwd_pp.cu"],
                  "sha256": "0fc8f248f8edfa9bb850c818a8d0491a4d0934cced9ead929024e61b5c60f791",
                  "bytes": 919404288 + 255160320},
-    # the loss GEMMs (one class, four epilogues): the schedule key is (seq_tile, None); the
-    # figure is the mean over one step's launches - per 8192-token tile the forward logits GEMM
-    # moves 2.20 GB, the backward's recompute 4.27 GB, dh 9.62 GB and dw 11.26 GB
-    "loss_gemm": {"workload": "llama8b_readout_s128k", "head_chunk": 8192, "seq_trunk": None,
-                  "files": ["context_parallelism_gb300/csrc/gemm_tc.cu",
-                            "context_parallelism_gb300/csrc/seqtile_api.cpp"],
-                  "sha256": "e310acce1166d860aa5bf37ccaed437662fc5e5b9a0f95cac746a5d2f2ff3e60",
-                  "bytes": 6836775836},
+    # the sequence-tiled GEMMs (one class, one kernel with several epilogues), one entry per
+    # workload; the schedule key is (seq_tile, None) and the figure is the mean over one
+    # step's launches. Loss, per 8192-token tile: forward logits 2.20 GB, backward recompute
+    # 4.27 GB, dh 9.62 GB, dw 11.23 GB. MLP: gate/up 0.76 GB, y 1.13 GB, recompute 1.25 GB,
+    # dg|du 1.56 GB, dWd 1.02 GB, dWgu 2.53 GB, dx 2.20 GB.
+    "loss_gemm": [
+        {"workload": "llama8b_readout_s128k", "head_chunk": 8192, "seq_trunk": None,
+         "files": ["context_parallelism_gb300/csrc/gemm_tc.cu",
+                   "context_parallelism_gb300/csrc/seqtile_api.cpp"],
+         "sha256": "4d0496c0f7fcdacca54efd5e1e437ac79d630b992a44c81970f71aebdda87797",
+         "bytes": 6831279392},
+        {"workload": "llama8b_mlp_s128k", "head_chunk": 8192, "seq_trunk": None,
+         "files": ["context_parallelism_gb300/csrc/gemm_tc.cu",
+                   "context_parallelism_gb300/csrc/seqtile_api.cpp"],
+         "sha256": "4d0496c0f7fcdacca54efd5e1e437ac79d630b992a44c81970f71aebdda87797",
+         "bytes": 1491132105},
+    ],
 }
 
 
@@ -103,12 +112,16 @@ def source_hash(files):
 def traffic_per_launch(kernel, workload, head_chunk, seq_trunk):
     """The captured DRAM bytes per launch of `kernel`, or None when the capture does not
     apply (other workload or schedule, kernel source changed since, or no capture)."""
-    t = TRAFFIC.get(kernel)
-    if not t or t["bytes"] is None:
-        return None
-    if (t["workload"], t["head_chunk"], t["seq_trunk"]) != (workload, head_chunk, seq_trunk):
-        return None
-    return t["bytes"] if source_hash(t["files"]) == t["sha256"] else None
+    entries = TRAFFIC.get(kernel) or []
+    if isinstance(entries, dict):
+        entries = [entries]
+    for t in entries:
+        if t["bytes"] is None:
+            continue
+        if (t["workload"], t["head_chunk"], t["seq_trunk"]) != (workload, head_chunk, seq_trunk):
+            continue
+        return t["bytes"] if source_hash(t["files"]) == t["sha256"] else None
+    return None
 
 
 def _peaks():
