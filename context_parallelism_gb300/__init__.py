@@ -57,11 +57,11 @@ SIGNATURES = {
     "upipe_profile_read": (_i, [ctypes.POINTER(KernelStat), _i]),
     "upipe_selftest_umma": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp]),
     "upipe_selftest_wait_timeout": (_i, [_i, _vp]),
-    "upipe_ce_workspace_bytes": (_sz, [_i64, _i, _i64, _i64, _i]),
+    "upipe_ce_workspace_bytes": (_sz, [_i64, _i, _i64, _i64, _i, _i]),
     "upipe_ce_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i64, _i, _i64, _i64, _vp, _sz, _vp]),
     "upipe_ce_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i, _i64, _i64, _vp, _sz,
                           _vp]),
-    "upipe_mlp_workspace_bytes": (_sz, [_i64, _i, _i, _i64, _i]),
+    "upipe_mlp_workspace_bytes": (_sz, [_i64, _i, _i, _i64, _i, _i]),
     "upipe_mlp_fwd": (_i, [_vp, _vp, _vp, _vp, _i64, _i, _i, _i64, _vp, _sz, _vp]),
     "upipe_mlp_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i, _i, _i64, _vp, _sz,
                            _vp]),
@@ -212,8 +212,8 @@ def upipe_selftest_wait_timeout(limit_us, stream=None):
            "upipe_selftest_wait_timeout")
 
 
-def upipe_ce_workspace_bytes(S, Dm, V, seq_tile, pass_=UPIPE_PASS_BOTH):
-    return int(_lib.upipe_ce_workspace_bytes(S, Dm, V, seq_tile, pass_))
+def upipe_ce_workspace_bytes(S, Dm, V, seq_tile, pass_=UPIPE_PASS_BOTH, host_mask=0):
+    return int(_lib.upipe_ce_workspace_bytes(S, Dm, V, seq_tile, pass_, int(host_mask)))
 
 
 def upipe_ce_fwd(h, w, target, loss, lse, S, Dm, V, seq_tile, workspace, workspace_bytes=None,
@@ -233,8 +233,8 @@ def upipe_ce_bwd(h, w, target, lse, dloss, dh, dw, S, Dm, V, seq_tile, workspace
     _check(st, "upipe_ce_bwd")
 
 
-def upipe_mlp_workspace_bytes(S, Dm, F, seq_tile, pass_=UPIPE_PASS_BOTH):
-    return int(_lib.upipe_mlp_workspace_bytes(S, Dm, F, seq_tile, pass_))
+def upipe_mlp_workspace_bytes(S, Dm, F, seq_tile, pass_=UPIPE_PASS_BOTH, host_mask=0):
+    return int(_lib.upipe_mlp_workspace_bytes(S, Dm, F, seq_tile, pass_, int(host_mask)))
 
 
 def upipe_mlp_fwd(x, w_gu, w_d, y, S, Dm, F, seq_tile, workspace, workspace_bytes=None,
@@ -332,71 +332,98 @@ def attention_backward(q, k, v, o, lse, dout, causal=True, head_chunk=None, seq_
     return dq, dk, dv
 
 
+def _tiled_device(*tensors):
+    import torch
+    for t in tensors:
+        if t is not None and t.is_cuda:
+            return t.device
+    return torch.device("cuda", torch.cuda.current_device())
+
+
+def _empty_like_on(shape, dtype, dev, on_host):
+    import torch
+    if on_host:
+        return torch.empty(shape, dtype=dtype, pin_memory=True)
+    return torch.empty(shape, dtype=dtype, device=dev)
+
+
 def ce_loss_forward(h, w, target, seq_tile=8192, workspace=None, stream=None):
     """loss, lse (float32 [S]) of the readout h [S, Dm] @ w[V, Dm]^T followed by token-level
     cross-entropy against target [S] (int64, negative = ignored), computed seq_tile tokens at
-    a time without storing logits."""
+    a time without storing logits. h may be a pinned host tensor (staged tile by tile)."""
     import torch
     S, Dm = h.shape
     V = w.shape[0]
-    loss = torch.empty(S, dtype=torch.float32, device=h.device)
-    lse = torch.empty(S, dtype=torch.float32, device=h.device)
-    need = upipe_ce_workspace_bytes(S, Dm, V, seq_tile, UPIPE_PASS_FWD)
+    dev = _tiled_device(w, target)
+    loss = torch.empty(S, dtype=torch.float32, device=dev)
+    lse = torch.empty(S, dtype=torch.float32, device=dev)
+    mask = 0 if h.is_cuda else UPIPE_HOST_ACT
+    need = upipe_ce_workspace_bytes(S, Dm, V, seq_tile, UPIPE_PASS_FWD, mask)
     if need == 0:
         upipe_ce_fwd(h, w, target, loss, lse, S, Dm, V, seq_tile, 0, 0, stream)
     if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=h.device)
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     upipe_ce_fwd(h, w, target, loss, lse, S, Dm, V, seq_tile, workspace, None, stream)
     return loss, lse
 
 
-def ce_loss_backward(h, w, target, lse, dloss, seq_tile=8192, workspace=None, stream=None):
+def ce_loss_backward(h, w, target, lse, dloss, seq_tile=8192, workspace=None, stream=None,
+                     dh_on_host=False):
     """dh (bf16 [S, Dm]) and dw (float32 [V, Dm]) of sum_i dloss[i] * loss[i] for the forward
-    above; lse is the forward's."""
+    above; lse is the forward's. h may be a pinned host tensor; dh_on_host returns dh as one."""
     import torch
     S, Dm = h.shape
     V = w.shape[0]
-    dh = torch.empty((S, Dm), dtype=h.dtype, device=h.device)
-    dw = torch.empty((V, Dm), dtype=torch.float32, device=h.device)
-    need = upipe_ce_workspace_bytes(S, Dm, V, seq_tile, UPIPE_PASS_BWD)
+    dev = _tiled_device(w, target)
+    dh = _empty_like_on((S, Dm), h.dtype, dev, dh_on_host)
+    dw = torch.empty((V, Dm), dtype=torch.float32, device=dev)
+    mask = UPIPE_HOST_ACT if (dh_on_host or not h.is_cuda) else 0
+    need = upipe_ce_workspace_bytes(S, Dm, V, seq_tile, UPIPE_PASS_BWD, mask)
     if need == 0:
         upipe_ce_bwd(h, w, target, lse, dloss, dh, dw, S, Dm, V, seq_tile, 0, 0, stream)
     if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=h.device)
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     upipe_ce_bwd(h, w, target, lse, dloss, dh, dw, S, Dm, V, seq_tile, workspace, None, stream)
     return dh, dw
 
 
-def mlp_forward(x, w_gu, w_d, seq_tile=8192, workspace=None, stream=None):
+def mlp_forward(x, w_gu, w_d, seq_tile=8192, workspace=None, stream=None, y_on_host=False):
     """y = (silu(x Wg^T) * x Wu^T) Wd^T for x [S, Dm], w_gu = [Wg; Wu] [2F, Dm], w_d [Dm, F]
-    (bf16), seq_tile tokens at a time."""
+    (bf16), seq_tile tokens at a time. x may be a pinned host tensor; y_on_host returns y as
+    one."""
     import torch
     S, Dm = x.shape
     F = w_d.shape[1]
-    y = torch.empty((S, Dm), dtype=x.dtype, device=x.device)
-    need = upipe_mlp_workspace_bytes(S, Dm, F, seq_tile, UPIPE_PASS_FWD)
+    dev = _tiled_device(w_gu)
+    y = _empty_like_on((S, Dm), x.dtype, dev, y_on_host)
+    mask = UPIPE_HOST_ACT if (y_on_host or not x.is_cuda) else 0
+    need = upipe_mlp_workspace_bytes(S, Dm, F, seq_tile, UPIPE_PASS_FWD, mask)
     if need == 0:
         upipe_mlp_fwd(x, w_gu, w_d, y, S, Dm, F, seq_tile, 0, 0, stream)
     if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     upipe_mlp_fwd(x, w_gu, w_d, y, S, Dm, F, seq_tile, workspace, None, stream)
     return y
 
 
-def mlp_backward(x, w_gu, w_d, dy, seq_tile=8192, workspace=None, stream=None):
+def mlp_backward(x, w_gu, w_d, dy, seq_tile=8192, workspace=None, stream=None,
+                 dx_on_host=False):
     """dx (bf16 [S, Dm]), dw_gu (float32 [2F, Dm]) and dw_d (float32 [Dm, F]) for the forward
-    above and the upstream gradient dy [S, Dm]."""
+    above and the upstream gradient dy [S, Dm]. x and dy may be pinned host tensors;
+    dx_on_host returns dx as one."""
     import torch
     S, Dm = x.shape
     F = w_d.shape[1]
-    dx = torch.empty_like(x)
-    dw_gu = torch.empty((2 * F, Dm), dtype=torch.float32, device=x.device)
-    dw_d = torch.empty((Dm, F), dtype=torch.float32, device=x.device)
-    need = upipe_mlp_workspace_bytes(S, Dm, F, seq_tile, UPIPE_PASS_BWD)
+    dev = _tiled_device(w_gu)
+    dx = _empty_like_on((S, Dm), x.dtype, dev, dx_on_host)
+    dw_gu = torch.empty((2 * F, Dm), dtype=torch.float32, device=dev)
+    dw_d = torch.empty((Dm, F), dtype=torch.float32, device=dev)
+    mask = UPIPE_HOST_ACT if (dx_on_host or not x.is_cuda or not dy.is_cuda) else 0
+    need = upipe_mlp_workspace_bytes(S, Dm, F, seq_tile, UPIPE_PASS_BWD, mask)
     if need == 0:
         upipe_mlp_bwd(x, w_gu, w_d, dy, dx, dw_gu, dw_d, S, Dm, F, seq_tile, 0, 0, stream)
     if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     upipe_mlp_bwd(x, w_gu, w_d, dy, dx, dw_gu, dw_d, S, Dm, F, seq_tile, workspace, None,
                   stream)
     return dx, dw_gu, dw_d

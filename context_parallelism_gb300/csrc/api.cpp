@@ -930,6 +930,7 @@ const char* upipe_status_string(int status) {
 const char* upipe_last_error_message(void) { return g_last_error.c_str(); }
 
 void upipe_shutdown(void) {
+  upipe::seqtile_shutdown();
   std::lock_guard<std::mutex> lk(g_mu);
   for (int i = 0; i < kMaxDev; ++i) {
     DevState& d = g_dev[i];

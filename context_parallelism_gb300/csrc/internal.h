@@ -159,6 +159,10 @@ cudaError_t launch_ce_merge(const float* part, int64_t part_stride, int n_parts,
 // Per-device state (streams, status word) for `dev`, created on first use; a upipe status.
 int device_status_word(int dev, uint32_t** err);
 
+// Releases the sequence-tiled calls' copy streams and events (seqtile_api.cpp); part of
+// upipe_shutdown.
+void seqtile_shutdown();
+
 // ---- self-tests (selftest.cu) --------------------------------------------------------------
 cudaError_t launch_selftest_umma(const void* a, const void* b, float* c, int N, int K,
                                  int a_mn, int b_mn, int a_manual, int lbo, int sbo,

@@ -207,8 +207,15 @@ void upipe_shutdown(void);
  * the calls reject): forward ceil(V/256) * T' * 8 + T' * 4 bytes with T' = min(seq_tile, S)
  * rounded up to 128; backward min(seq_tile, S) * V * 2 bytes; each rounded up to 256.
  * Asynchronous on `stream`, like the attention calls.
+ * Host activations: h (and dh) may instead be PINNED host memory. The call then stages each
+ * tile of h into one of two device slots on a library inbound copy stream, two tiles ahead,
+ * and copies each tile of dh out on an outbound copy stream while the next tile computes;
+ * `stream` completes after the last copy. The workspace must then be sized with host_mask =
+ * UPIPE_HOST_ACT, which adds 2 (forward) or 4 (backward) slots of min(seq_tile, S) * Dm * 2
+ * bytes, each rounded up to 256 (host_mask 0: device activations only; other bits: 0 bytes).
  */
-size_t upipe_ce_workspace_bytes(int64_t S, int Dm, int64_t V, int64_t seq_tile, int pass);
+size_t upipe_ce_workspace_bytes(int64_t S, int Dm, int64_t V, int64_t seq_tile, int pass,
+                                int host_mask);
 int upipe_ce_fwd(const void* h, const void* w, const int64_t* target, float* loss, float* lse,
                  int64_t S, int Dm, int64_t V, int64_t seq_tile, void* workspace,
                  size_t workspace_bytes, void* stream);
@@ -233,9 +240,14 @@ int upipe_ce_bwd(const void* h, const void* w, const int64_t* target, const floa
  * run on the tensor cores (bf16 operands, fp32 accumulation); a, g, u, dg, du are rounded to
  * bf16 between GEMMs. Workspace (upipe_mlp_workspace_bytes): forward T*F*2 bytes (a),
  * backward 5*T*F*2 (a, g|u, dg|du), T = min(seq_tile, S), each buffer rounded up to 256;
- * pass BOTH is the backward's.
+ * pass BOTH is the larger of the two.
+ * Host activations: x, y, dy and dx may each instead be PINNED host memory, staged tile by
+ * tile as for the loss (inputs two tiles ahead on an inbound copy stream, outputs copied out
+ * while the next tile computes). host_mask = UPIPE_HOST_ACT then adds two slots of
+ * T * Dm * 2 bytes for each of x and y (forward) or x, dy and dx (backward).
  */
-size_t upipe_mlp_workspace_bytes(int64_t S, int Dm, int F, int64_t seq_tile, int pass);
+size_t upipe_mlp_workspace_bytes(int64_t S, int Dm, int F, int64_t seq_tile, int pass,
+                                 int host_mask);
 int upipe_mlp_fwd(const void* x, const void* w_gu, const void* w_d, void* y, int64_t S, int Dm,
                   int F, int64_t seq_tile, void* workspace, size_t workspace_bytes,
                   void* stream);

@@ -190,6 +190,12 @@ def test_loss_workspace_matches_formula(S, Dm, V, T):
     assert up.upipe_ce_workspace_bytes(S, Dm, V, T, up.UPIPE_PASS_FWD) == fwd
     assert up.upipe_ce_workspace_bytes(S, Dm, V, T, up.UPIPE_PASS_BWD) == bwd
     assert up.upipe_ce_workspace_bytes(S, Dm, V, T, up.UPIPE_PASS_BOTH) == max(fwd, bwd)
+    # host activations: two slots of a tile of h (forward), of h and dh (backward)
+    slot = (min(T, S) * Dm * 2 + 255) // 256 * 256
+    ha = up.UPIPE_HOST_ACT
+    assert up.upipe_ce_workspace_bytes(S, Dm, V, T, up.UPIPE_PASS_FWD, ha) == fwd + 2 * slot
+    assert up.upipe_ce_workspace_bytes(S, Dm, V, T, up.UPIPE_PASS_BWD, ha) == bwd + 4 * slot
+    assert up.upipe_ce_workspace_bytes(S, Dm, V, T, up.UPIPE_PASS_BWD, up.UPIPE_HOST_KV) == 0
 
 
 def test_loss_workspace_is_bounded_by_the_tile_not_the_sequence():
@@ -230,6 +236,10 @@ def test_mlp_workspace_matches_formula(S, Dm, F, T):
     bwd = al(tf) + 2 * al(2 * tf)
     assert up.upipe_mlp_workspace_bytes(S, Dm, F, T, up.UPIPE_PASS_BWD) == bwd
     assert up.upipe_mlp_workspace_bytes(S, Dm, F, T, up.UPIPE_PASS_BOTH) == bwd
+    slot = al(Tt * Dm * 2)
+    ha = up.UPIPE_HOST_ACT
+    assert up.upipe_mlp_workspace_bytes(S, Dm, F, T, up.UPIPE_PASS_FWD, ha) == al(tf) + 4 * slot
+    assert up.upipe_mlp_workspace_bytes(S, Dm, F, T, up.UPIPE_PASS_BWD, ha) == bwd + 6 * slot
     # bounded by the tile: the same at 32x the sequence
     S1 = max(S, T)
     assert up.upipe_mlp_workspace_bytes(32 * S1, Dm, F, T, up.UPIPE_PASS_BWD) == \

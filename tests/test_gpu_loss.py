@@ -114,6 +114,25 @@ def test_loss_rejects_bad_shapes_and_small_workspace():
     assert e.value.status == up.UPIPE_ERR_WORKSPACE_TOO_SMALL
 
 
+@pytest.mark.parametrize("S,T", [(1000, 256), (384, 128), (100, 128)])
+def test_host_activations_equal_device(S, T):
+    """h in pinned host memory (staged tile by tile) and dh returned to pinned host memory
+    give bitwise the results of device-resident h and dh: the staging moves bytes only."""
+    lw = LOSS_WORKLOADS["readout_small"].with_(S=S, seed=47 + S)
+    h, w, t, _ = make_loss_inputs(lw, "cpu")
+    g = _random_g(S, lw.seed)
+    ref = _run(h, w, t, g, T)
+    wg, tg, gg = w.cuda(), t.cuda(), g.cuda()
+    hh = torch.empty(h.shape, dtype=h.dtype, pin_memory=True)
+    hh.copy_(h)
+    loss, lse = up.ce_loss_forward(hh, wg, tg, seq_tile=T)
+    dh, dw = up.ce_loss_backward(hh, wg, tg, lse, gg, seq_tile=T, dh_on_host=True)
+    up.upipe_sync_status()
+    assert not dh.is_cuda and dh.is_pinned()
+    assert torch.equal(loss, ref[0]) and torch.equal(lse, ref[1])
+    assert torch.equal(dh, ref[2].cpu()) and torch.equal(dw, ref[3])
+
+
 @pytest.mark.slow
 def test_loss_full_size_sampled():
     """The measured configuration (S = 128K tokens, Dm 4096, V 128256, tiles of 8192) in the

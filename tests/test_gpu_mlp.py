@@ -70,6 +70,42 @@ def test_mlp_rejects_bad_shapes():
     assert e.value.status == up.UPIPE_ERR_UNSUPPORTED
 
 
+def _pinned(t):
+    out = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+    out.copy_(t)
+    return out
+
+
+@pytest.mark.parametrize("S,T,which", [(1000, 256, "all"), (600, 128, "x"), (300, 128, "dy"),
+                                       (100, 128, "outputs")])
+def test_mlp_host_activations_equal_device(S, T, which):
+    """Any of x, dy (inputs) and y, dx (outputs) in pinned host memory, staged tile by tile,
+    give bitwise the device-resident results."""
+    mw = MLP_WORKLOADS["mlp_small"].with_(S=S, seed=50 + S)
+    x, w_gu, w_d, dy = make_mlp_inputs(mw, "cpu")
+    ref = _run(x, w_gu, w_d, dy, T)
+    wg, wd = w_gu.cuda(), w_d.cuda()
+    xi = _pinned(x) if which in ("all", "x") else x.cuda()
+    dyi = _pinned(dy) if which in ("all", "dy") else dy.cuda()
+    out_host = which in ("all", "outputs")
+    y = up.mlp_forward(xi, wg, wd, seq_tile=T, y_on_host=out_host)
+    dx, dw_gu, dw_d = up.mlp_backward(xi, wg, wd, dyi, seq_tile=T, dx_on_host=out_host)
+    up.upipe_sync_status()
+    assert y.is_cuda != out_host and dx.is_cuda != out_host
+    assert torch.equal(y.cpu(), ref[0].cpu()) and torch.equal(dx.cpu(), ref[1].cpu())
+    assert torch.equal(dw_gu, ref[2]) and torch.equal(dw_d, ref[3])
+
+
+def test_mlp_host_activations_need_the_staging_workspace():
+    mw = MLP_WORKLOADS["mlp_small"].with_(S=512)
+    x, w_gu, w_d, _ = make_mlp_inputs(mw, "cpu")
+    dev_ws = up.upipe_mlp_workspace_bytes(512, mw.Dm, mw.F, 256, up.UPIPE_PASS_FWD)
+    ws = torch.empty(dev_ws, dtype=torch.uint8, device="cuda")
+    with pytest.raises(up.UpipeError) as e:
+        up.mlp_forward(_pinned(x), w_gu.cuda(), w_d.cuda(), seq_tile=256, workspace=ws)
+    assert e.value.status == up.UPIPE_ERR_WORKSPACE_TOO_SMALL
+
+
 @pytest.mark.slow
 def test_mlp_full_size_sampled():
     """The measured configuration (S = 128K, Dm 4096, F 14336, tiles of 8192) in the launch
