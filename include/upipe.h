@@ -30,8 +30,10 @@
  *   - `stream` is a cudaStream_t (NULL = legacy default stream). All work is enqueued on it
  *     and calls return before the GPU finishes (asynchronous, like a kernel launch).
  *   - Ownership: the caller owns every buffer, including the workspace. Per call the library
- *     allocates no device memory. Per device it lazily creates two internal copy streams,
- *     a few events and a 256-byte device status word; upipe_shutdown() releases them.
+ *     allocates no device memory. Per device it lazily creates two internal copy streams for
+ *     the attention calls and two for the sequence-tiled calls (used only when activations
+ *     are pinned host memory), a few events and a 256-byte device status word;
+ *     upipe_shutdown() releases them.
  *   - Errors: all arguments are validated before anything is enqueued; on an error nothing
  *     is launched and a status code is returned (see upipe_status). A device-side bounded
  *     wait that expires sets the device status word and the kernel exits early; the host
