@@ -61,25 +61,24 @@ struct GLayout {
   static constexpr int kBytes = kAbort + 4 + 1024;
 };
 
-// Tile order. m_fastest: groups of group_m M tiles (all of them when group_m <= 0) are walked
+// Tile order. m_fastest: groups of `group` M tiles (all of them when group <= 0) are walked
 // M tile first, then N tile, group after group - the CTAs in flight then share a few B strips
-// and at most group_m A strips, which bounds the set of operand bytes that has to stay in L2.
-// Otherwise N tile first.
-__device__ __forceinline__ void tile_coords(int t, int mt_n, int nt_n, int m_fastest,
-                                            int group_m, int& mt, int& nt) {
-  if (m_fastest) {
-    const int gm = (group_m > 0 && group_m < mt_n) ? group_m : mt_n;
-    const int per_group = gm * nt_n;
-    const int grp = t / per_group;
-    const int rem = t - grp * per_group;
-    const int m0 = grp * gm;
-    const int rows = min(gm, mt_n - m0);
-    mt = m0 + rem % rows;
-    nt = rem / rows;
-  } else {
-    nt = t % nt_n;
-    mt = t / nt_n;
-  }
+// and at most `group` A strips, which bounds the set of operand bytes that has to stay in L2.
+// Otherwise the same with the roles of M and N exchanged (groups of N tiles, N tile first).
+__device__ __forceinline__ void tile_coords(int t, int mt_n, int nt_n, int m_fastest, int group,
+                                            int& mt, int& nt) {
+  const int fast_n = m_fastest ? mt_n : nt_n;  // tiles along the fast dimension
+  const int slow_n = m_fastest ? nt_n : mt_n;
+  const int g = (group > 0 && group < fast_n) ? group : fast_n;
+  const int per_group = g * slow_n;
+  const int grp = t / per_group;
+  const int rem = t - grp * per_group;
+  const int f0 = grp * g;
+  const int width = min(g, fast_n - f0);
+  const int f = f0 + rem % width;
+  const int sl = rem / width;
+  mt = m_fastest ? f : sl;
+  nt = m_fastest ? sl : f;
 }
 
 __device__ __forceinline__ uint4 pack8(const float* x) {

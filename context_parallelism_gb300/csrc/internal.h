@@ -123,7 +123,7 @@ enum : int {
 struct GemmArgs {
   int M, N, K;            // N % 64 == 0; M, K any (tensor maps zero-fill past the edges)
   int m_fastest;          // tile order: 1 walks M tiles first (shares a B strip), 0 N tiles first
-  int group_m;            // with m_fastest: M tiles per group (<= 0: all), see tile_coords
+  int group_m;            // tiles of the fast dimension per group (<= 0: all), see tile_coords
   void* c;                // STORE: bf16 [M][ldc]; ACC_F32: fp32 [M][ldc]; CE_BWD: bf16 dlogits
   int64_t ldc;
   int accumulate;         // ACC_F32: add into c instead of overwriting

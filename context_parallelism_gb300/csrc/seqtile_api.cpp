@@ -52,6 +52,12 @@ int lfail(int status, const char* fmt, ...) {
 #ifndef UPIPE_CE_GROUP_M
 #define UPIPE_CE_GROUP_M 32
 #endif
+// N tiles (256 output columns each) walked together by the weight-gradient GEMMs (dw of the
+// loss, dWgu of the MLP), whose B operand is the token tile: 8 column strips of it (8 x 256 x
+// T x 2 bytes: 32 MiB at T = 8192) stay in L2 while the A strips stream past them.
+#ifndef UPIPE_WG_GROUP_N
+#define UPIPE_WG_GROUP_N 8
+#endif
 
 constexpr size_t kAl = 256;
 inline size_t al(size_t x) { return (x + kAl - 1) / kAl * kAl; }
@@ -493,6 +499,7 @@ int upipe_ce_bwd(const void* h, const void* w, const int64_t* target, const floa
     y.N = Dm;
     y.K = static_cast<int>(Mc);
     y.m_fastest = 0;
+    y.group_m = UPIPE_WG_GROUP_N;
     y.c = dw;
     y.ldc = Dm;
     y.accumulate = r0 > 0 ? 1 : 0;
@@ -671,6 +678,7 @@ int upipe_mlp_bwd(const void* x, const void* w_gu, const void* w_d, const void* 
     wg.N = Dm;
     wg.K = static_cast<int>(Mc);
     wg.m_fastest = 0;
+    wg.group_m = UPIPE_WG_GROUP_N;
     wg.c = dw_gu;
     wg.ldc = Dm;
     wg.accumulate = r0 > 0 ? 1 : 0;
