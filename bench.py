@@ -82,20 +82,20 @@ TRAFFIC = {
                  "bytes": 919404288 + 255160320},
     # the sequence-tiled GEMMs (one class, one kernel with several epilogues), one entry per
     # workload; the schedule key is (seq_tile, None) and the figure is the mean over one
-    # step's launches. Loss, per 8192-token tile: forward logits 2.20 GB, backward recompute
-    # 4.27 GB, dh 9.62 GB, dw 11.23 GB. MLP: gate/up 0.76 GB, y 1.13 GB, recompute 1.25 GB,
-    # dg|du 1.56 GB, dWd 1.02 GB, dWgu 2.53 GB, dx 2.20 GB.
+    # step's launches. Loss, per 8192-token tile: forward logits 2.21 GB, backward recompute
+    # 4.28 GB, dh 8.47 GB, dw 8.71 GB. MLP: gate/up 0.76 GB, y 1.00 GB, recompute 1.24 GB,
+    # dg|du 1.52 GB, dWd 1.02 GB, dWgu 1.97 GB, dx 1.94 GB.
     "loss_gemm": [
         {"workload": "llama8b_readout_s128k", "head_chunk": 8192, "seq_trunk": None,
          "files": ["context_parallelism_gb300/csrc/gemm_tc.cu",
                    "context_parallelism_gb300/csrc/seqtile_api.cpp"],
-         "sha256": "4d0496c0f7fcdacca54efd5e1e437ac79d630b992a44c81970f71aebdda87797",
-         "bytes": 6831279392},
+         "sha256": "1c2aafc93fc6c36438f0cc82aa80e78d9c57194496da00888c54cb92cdf445ab",
+         "bytes": 5913879764},
         {"workload": "llama8b_mlp_s128k", "head_chunk": 8192, "seq_trunk": None,
          "files": ["context_parallelism_gb300/csrc/gemm_tc.cu",
                    "context_parallelism_gb300/csrc/seqtile_api.cpp"],
-         "sha256": "4d0496c0f7fcdacca54efd5e1e437ac79d630b992a44c81970f71aebdda87797",
-         "bytes": 1491132105},
+         "sha256": "1c2aafc93fc6c36438f0cc82aa80e78d9c57194496da00888c54cb92cdf445ab",
+         "bytes": 1350233074},
     ],
 }
 

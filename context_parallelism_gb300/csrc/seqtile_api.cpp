@@ -58,6 +58,13 @@ int lfail(int status, const char* fmt, ...) {
 #ifndef UPIPE_WG_GROUP_N
 #define UPIPE_WG_GROUP_N 8
 #endif
+// N tiles walked together by the output GEMMs with a long reduction (dh = dlogits w, y = a Wd^T,
+// dx = (dg | du) [Wg; Wu]): each wave of CTAs streams its A strips (128 token rows each) and
+// its B strips (256 output columns each) along the whole reduction, so a wave of 19 x 8 tiles
+// moves fewer bytes than one of 9.5 x 16 when a B strip is twice an A strip.
+#ifndef UPIPE_ST_GROUP_N
+#define UPIPE_ST_GROUP_N 8
+#endif
 
 constexpr size_t kAl = 256;
 inline size_t al(size_t x) { return (x + kAl - 1) / kAl * kAl; }
@@ -489,6 +496,7 @@ int upipe_ce_bwd(const void* h, const void* w, const int64_t* target, const floa
     x.N = Dm;
     x.K = static_cast<int>(V);
     x.m_fastest = 0;
+    x.group_m = UPIPE_ST_GROUP_N;
     x.c = out[0].rows(s, r0);
     x.ldc = Dm;
     x.err = err;
@@ -574,6 +582,7 @@ int upipe_mlp_fwd(const void* x, const void* w_gu, const void* w_d, void* y, int
     o.N = Dm;
     o.K = F;
     o.m_fastest = 0;
+    o.group_m = UPIPE_ST_GROUP_N;
     o.c = out[0].rows(s, r0);
     o.ldc = Dm;
     o.err = err;
@@ -690,6 +699,7 @@ int upipe_mlp_bwd(const void* x, const void* w_gu, const void* w_d, const void* 
     gx.N = Dm;
     gx.K = static_cast<int>(F2);
     gx.m_fastest = 0;
+    gx.group_m = UPIPE_ST_GROUP_N;
     gx.c = out[0].rows(s, r0);
     gx.ldc = Dm;
     gx.err = err;
