@@ -215,6 +215,10 @@ void upipe_shutdown(void);
  * `stream` completes after the last copy. The workspace must then be sized with host_mask =
  * UPIPE_HOST_ACT, which adds 2 (forward) or 4 (backward) slots of min(seq_tile, S) * Dm * 2
  * bytes, each rounded up to 256 (host_mask 0: device activations only; other bits: 0 bytes).
+ * Calls that stage host activations share one pair of copy streams and their events per
+ * device: two such calls whose work could overlap (different streams, unordered threads) must
+ * be serialised by the caller. Calls with device activations only have no such restriction
+ * beyond their workspaces being distinct.
  */
 size_t upipe_ce_workspace_bytes(int64_t S, int Dm, int64_t V, int64_t seq_tile, int pass,
                                 int host_mask);
