@@ -53,6 +53,7 @@ SIGNATURES = {
     "upipe_last_error_message": (ctypes.c_char_p, []),
     "upipe_shutdown": (None, []),
     "upipe_launch_count": (_u64, []),
+    "upipe_debug_fail_copy_after": (_i, [_i]),
     "upipe_profile_enable": (_i, [_i]),
     "upipe_profile_read": (_i, [ctypes.POINTER(KernelStat), _i]),
     "upipe_selftest_umma": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp]),
@@ -187,6 +188,11 @@ def upipe_shutdown():
 
 def upipe_launch_count():
     return int(_lib.upipe_launch_count())
+
+
+def upipe_debug_fail_copy_after(n):
+    """Test hook: the n-th staging copy from now on fails (0 disarms)."""
+    _check(_lib.upipe_debug_fail_copy_after(int(n)), "upipe_debug_fail_copy_after")
 
 
 def upipe_profile_enable(on=True):

@@ -342,6 +342,7 @@ int stage_trunk(const Plan& p, const void* src, uint8_t* slot, int kvh0, int64_t
       const uint8_t* s = static_cast<const uint8_t*>(src) +
                          ((static_cast<size_t>(b) * p.S + t0) * p.Hkv + kvh0 + c) * row;
       uint8_t* d = slot + (static_cast<size_t>(b) * p.kc + c) * Tn * row;
+      if (staging_copy_fails()) return fail(UPIPE_ERR_CUDA, "injected staging copy failure");
       UPIPE_CUDA(cudaMemcpy2DAsync(d, row, s, static_cast<size_t>(p.Hkv) * row, row,
                                    static_cast<size_t>(Tn), cudaMemcpyHostToDevice, copy));
     }
@@ -356,6 +357,7 @@ int unstage_trunk(const Plan& p, const uint8_t* slot, void* dst, int kvh0, int64
   for (int b = 0; b < p.B; ++b) {
     uint8_t* d = static_cast<uint8_t*>(dst) + ((static_cast<size_t>(b) * p.S + t0) * p.Hkv + kvh0) * row;
     const uint8_t* s = slot + static_cast<size_t>(b) * Tn * w;
+    if (staging_copy_fails()) return fail(UPIPE_ERR_CUDA, "injected staging copy failure");
     UPIPE_CUDA(cudaMemcpy2DAsync(d, static_cast<size_t>(p.Hkv) * row, s, w, w,
                                  static_cast<size_t>(Tn), cudaMemcpyDeviceToHost, copy));
   }
@@ -372,6 +374,7 @@ int stage_heads(const void* src, void* dst, int B, int64_t S, int H, int D, int 
       const uint8_t* s = static_cast<const uint8_t*>(src) +
                          (static_cast<size_t>(b) * S * H + h0 + c) * row;
       uint8_t* d = static_cast<uint8_t*>(dst) + (static_cast<size_t>(b) * hc + c) * S * row;
+      if (staging_copy_fails()) return fail(UPIPE_ERR_CUDA, "injected staging copy failure");
       UPIPE_CUDA(cudaMemcpy2DAsync(d, row, s, static_cast<size_t>(H) * row, row,
                                    static_cast<size_t>(S), cudaMemcpyHostToDevice, copy));
     }
@@ -386,6 +389,7 @@ int unstage_heads(const void* stg, void* dst, int B, int64_t S, int H, int D, in
   for (int b = 0; b < B; ++b) {
     uint8_t* d = static_cast<uint8_t*>(dst) + (static_cast<size_t>(b) * S * H + h0) * row;
     const uint8_t* s = static_cast<const uint8_t*>(stg) + static_cast<size_t>(b) * S * w;
+    if (staging_copy_fails()) return fail(UPIPE_ERR_CUDA, "injected staging copy failure");
     UPIPE_CUDA(cudaMemcpy2DAsync(d, static_cast<size_t>(H) * row, s, w, w,
                                  static_cast<size_t>(S), cudaMemcpyDeviceToHost, copy));
   }
@@ -436,6 +440,23 @@ struct Stager {
 };
 
 }  // namespace
+
+namespace {
+std::atomic<int> g_fail_copy_after{0};  // 0: disarmed; n: the n-th staging copy from now fails
+}  // namespace
+
+bool staging_copy_fails() {
+  int n = g_fail_copy_after.load(std::memory_order_relaxed);
+  while (n > 0) {
+    if (g_fail_copy_after.compare_exchange_weak(n, n - 1)) return n == 1;
+  }
+  return false;
+}
+
+int upipe_debug_arm_copy_failure(int n) {
+  g_fail_copy_after.store(n);
+  return UPIPE_OK;
+}
 
 int device_status_word(int dev, uint32_t** err) {
   if (dev < 0 || dev >= kMaxDev) return fail(UPIPE_ERR_INVALID_ARG, "device %d out of range", dev);
@@ -959,6 +980,12 @@ void upipe_shutdown(void) {
 }
 
 uint64_t upipe_launch_count(void) { return g_launches.load(); }
+
+int upipe_debug_fail_copy_after(int n) {
+  g_last_error.clear();
+  if (n < 0) return fail(UPIPE_ERR_INVALID_ARG, "n must be >= 0");
+  return upipe::upipe_debug_arm_copy_failure(n);
+}
 
 int upipe_profile_enable(int on) {
   g_profile.store(on != 0);

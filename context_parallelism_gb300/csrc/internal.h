@@ -163,6 +163,11 @@ int device_status_word(int dev, uint32_t** err);
 // upipe_shutdown.
 void seqtile_shutdown();
 
+// Test hook (upipe_debug_fail_copy_after): true when the staging copy about to be issued is the
+// one armed to fail; the caller then returns UPIPE_ERR_CUDA without issuing it. Counts every
+// host<->device staging copy of every call while armed.
+bool staging_copy_fails();
+
 // ---- self-tests (selftest.cu) --------------------------------------------------------------
 cudaError_t launch_selftest_umma(const void* a, const void* b, float* c, int N, int K,
                                  int a_mn, int b_mn, int a_manual, int lbo, int sbo,

@@ -186,10 +186,12 @@ int run_tiles(int64_t S, int64_t T, const Act* ins, int n_in, const Act* outs, i
     const int64_t r0 = i * T, Mc = (S - r0) < T ? (S - r0) : T;
     if (i >= 2) LOSS_CUDA(cudaStreamWaitEvent(sg->in, sg->in_free[s], 0));
     for (int k = 0; k < n_in; ++k)
-      if (ins[k].host)
+      if (ins[k].host) {
+        if (staging_copy_fails()) return lfail(UPIPE_ERR_CUDA, "injected staging copy failure");
         LOSS_CUDA(cudaMemcpyAsync(ins[k].slot[s],
                                   static_cast<const uint8_t*>(ins[k].base) + r0 * ins[k].row_bytes,
                                   Mc * ins[k].row_bytes, cudaMemcpyHostToDevice, sg->in));
+      }
     LOSS_CUDA(cudaEventRecord(sg->in_ready[s], sg->in));
     return UPIPE_OK;
   };
@@ -212,11 +214,13 @@ int run_tiles(int64_t S, int64_t T, const Act* ins, int n_in, const Act* outs, i
       LOSS_CUDA(cudaEventRecord(sg->out_done[s], stream));
       LOSS_CUDA(cudaStreamWaitEvent(sg->out, sg->out_done[s], 0));
       for (int k = 0; k < n_out; ++k)
-        if (outs[k].host)
+        if (outs[k].host) {
+          if (staging_copy_fails()) return lfail(UPIPE_ERR_CUDA, "injected staging copy failure");
           LOSS_CUDA(cudaMemcpyAsync(const_cast<uint8_t*>(static_cast<const uint8_t*>(outs[k].base)) +
                                         r0 * outs[k].row_bytes,
                                     outs[k].slot[s], Mc * outs[k].row_bytes,
                                     cudaMemcpyDeviceToHost, sg->out));
+        }
       LOSS_CUDA(cudaEventRecord(sg->out_free[s], sg->out));
     }
   }

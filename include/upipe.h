@@ -281,6 +281,17 @@ typedef struct {
   uint64_t launches; /* launches recorded */
 } upipe_kernel_stat;
 
+/*
+ * Test hook for failure handling: n >= 1 arms the n-th host<->device staging copy issued from
+ * now on (K/V trunks, dK/dV trunks, head-group activations, tiles of the sequence-tiled
+ * calls; counted across calls and threads) to fail as if its copy call had returned an error:
+ * the call that would issue it returns UPIPE_ERR_CUDA ("injected staging copy failure")
+ * without issuing it. Work that call already enqueued stays enqueued and completes; its
+ * outputs are undefined. Fires once, then disarms; 0 disarms; n < 0 is UPIPE_ERR_INVALID_ARG.
+ * Touches no device.
+ */
+int upipe_debug_fail_copy_after(int n);
+
 /* Total kernel launches made by this library in this process (all classes). */
 uint64_t upipe_launch_count(void);
 

@@ -258,3 +258,9 @@ def test_mlp_calls_validate_before_device_access():
     st = up._lib.upipe_mlp_bwd(None, None, None, None, None, None, None, 128, 64, 192, 128,
                                None, 0, None)
     assert st == up.UPIPE_ERR_UNSUPPORTED
+
+
+def test_copy_failure_hook_arms_and_validates_without_gpu():
+    assert up._lib.upipe_debug_fail_copy_after(-1) == up.UPIPE_ERR_INVALID_ARG
+    up.upipe_debug_fail_copy_after(5)
+    up.upipe_debug_fail_copy_after(0)  # disarmed again
