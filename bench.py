@@ -699,8 +699,36 @@ def _loss_spec(a, dev, up):
             "h in pinned host memory staged tile by tile by the library (dh likewise out); " \
             "targets in and the per-token loss out by the caller; w and dw on the device"
 
+    def fused_measure(steps, warmup):
+        # the one-call forward + backward for a dloss known up front: same results, no logits
+        # recompute; timed on its own, same inputs
+        wbf = up.upipe_ce_workspace_bytes(S, Dm, V, T, up.UPIPE_PASS_FUSED)
+        wsf = torch.empty(wbf, dtype=torch.uint8, device=dev)
+
+        def step():
+            up.upipe_ce_fwd_bwd(h, w, t, g, loss, lse, dh, dw, S, Dm, V, T, wsf, wbf, stream)
+        for _ in range(warmup):
+            step()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        up.upipe_sync_status(stream)
+        ms = e0.elapsed_time(e1) / steps
+        executed = 3 * lw.flops_fwd()  # logits, dh and dw GEMMs
+        return {"fused": {"ms_per_step": ms, "tokens_per_s": S / (ms / 1e3),
+                          "tflops_executed": executed / (ms / 1e3) / 1e12,
+                          "workspace_gb": wbf / 1e9,
+                          "method": "upipe_ce_fwd_bwd: the forward keeps fp32 logits, dlogits "
+                                    "from them (no recompute GEMM); TFLOP/s over the three "
+                                    "GEMMs executed"}}
+
     return {
         "metric": LOSS_METRIC, "name": lw.name, "seq_tile": T, "host_setup": host_setup,
+        "extra_measure": fused_measure,
         "fwd": lambda: up.upipe_ce_fwd(h, w, t, loss, lse, S, Dm, V, T, ws, ws_bytes, stream),
         "bwd": lambda: up.upipe_ce_bwd(h, w, t, lse, g, dh, dw, S, Dm, V, T, ws, ws_bytes, stream),
         "f_fwd": lw.flops_fwd(), "f_bwd": lw.flops_bwd(), "ws_bytes": ws_bytes,
@@ -831,6 +859,10 @@ def run_tiled(a, make_spec):
                 "traffic_unit": "bytes per launch"}
     kernels = {k: {"ms_per_step": tm / a.steps, "launches_per_step": n / a.steps}
                for k, (tm, n) in prof.items() if n}
+    extra_measured = sp["extra_measure"](a.steps, a.warmup) if "extra_measure" in sp else {}
+    if "fused" in extra_measured:
+        extra_measured["fused"]["speedup_vs_two_calls"] = \
+            (t_max / a.steps) / extra_measured["fused"]["ms_per_step"]
     config = dict(sp["config"])
     config["parallelism"] = "replicas" if world > 1 else "single"
     line = {
@@ -843,6 +875,7 @@ def run_tiled(a, make_spec):
         "frac_of_bf16_peak": value / world / peak, "peak_tflops": peak,
         "workspace_gb": sp["ws_bytes"] / 1e9, **sp["extra"],
         "roofline": roofline, "kernels": kernels, "gpu_launches": int(launches), "clocks": clk,
+        **extra_measured,
     }
     if not a.no_e2e:
         # host buffers in (every input), every output out, each step

@@ -24,7 +24,7 @@ UPIPE_ERR_WORKSPACE_TOO_SMALL = 3
 UPIPE_ERR_CUDA = 4
 UPIPE_ERR_TIMEOUT = 5
 
-UPIPE_PASS_FWD, UPIPE_PASS_BWD, UPIPE_PASS_BOTH = 0, 1, 2
+UPIPE_PASS_FWD, UPIPE_PASS_BWD, UPIPE_PASS_BOTH, UPIPE_PASS_FUSED = 0, 1, 2, 3
 UPIPE_HOST_KV, UPIPE_HOST_ACT = 1, 2
 
 KERNEL_CLASSES = ["layout", "attn_fwd", "bwd_pre", "attn_bwd", "dq_convert", "other",
@@ -62,6 +62,8 @@ SIGNATURES = {
     "upipe_ce_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i64, _i, _i64, _i64, _vp, _sz, _vp]),
     "upipe_ce_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i, _i64, _i64, _vp, _sz,
                           _vp]),
+    "upipe_ce_fwd_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i, _i64, _i64, _vp,
+                              _sz, _vp]),
     "upipe_mlp_workspace_bytes": (_sz, [_i64, _i, _i, _i64, _i, _i]),
     "upipe_mlp_fwd": (_i, [_vp, _vp, _vp, _vp, _i64, _i, _i, _i64, _vp, _sz, _vp]),
     "upipe_mlp_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i, _i, _i64, _vp, _sz,
@@ -239,6 +241,15 @@ def upipe_ce_bwd(h, w, target, lse, dloss, dh, dw, S, Dm, V, seq_tile, workspace
     _check(st, "upipe_ce_bwd")
 
 
+def upipe_ce_fwd_bwd(h, w, target, dloss, loss, lse, dh, dw, S, Dm, V, seq_tile, workspace,
+                     workspace_bytes=None, stream=None):
+    wb = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    st = _lib.upipe_ce_fwd_bwd(_ptr(h), _ptr(w), _ptr(target), _ptr(dloss), _ptr(loss),
+                               _ptr(lse), _ptr(dh), _ptr(dw), S, Dm, V, seq_tile,
+                               _ptr(workspace), wb, _stream(stream, h, loss, workspace))
+    _check(st, "upipe_ce_fwd_bwd")
+
+
 def upipe_mlp_workspace_bytes(S, Dm, F, seq_tile, pass_=UPIPE_PASS_BOTH, host_mask=0):
     return int(_lib.upipe_mlp_workspace_bytes(S, Dm, F, seq_tile, pass_, int(host_mask)))
 
@@ -391,6 +402,30 @@ def ce_loss_backward(h, w, target, lse, dloss, seq_tile=8192, workspace=None, st
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     upipe_ce_bwd(h, w, target, lse, dloss, dh, dw, S, Dm, V, seq_tile, workspace, None, stream)
     return dh, dw
+
+
+def ce_loss_fused(h, w, target, dloss, seq_tile=8192, workspace=None, stream=None,
+                  dh_on_host=False):
+    """loss, lse, dh, dw in one call when the upstream gradient dloss is known up front (the
+    loss is the last operation). Bitwise the results of ce_loss_forward + ce_loss_backward,
+    without the backward's logits recompute; needs seq_tile * V * 6 more bytes of workspace."""
+    import torch
+    S, Dm = h.shape
+    V = w.shape[0]
+    dev = _tiled_device(w, target)
+    loss = torch.empty(S, dtype=torch.float32, device=dev)
+    lse = torch.empty(S, dtype=torch.float32, device=dev)
+    dh = _empty_like_on((S, Dm), h.dtype, dev, dh_on_host)
+    dw = torch.empty((V, Dm), dtype=torch.float32, device=dev)
+    mask = UPIPE_HOST_ACT if (dh_on_host or not h.is_cuda) else 0
+    need = upipe_ce_workspace_bytes(S, Dm, V, seq_tile, UPIPE_PASS_FUSED, mask)
+    if need == 0:
+        upipe_ce_fwd_bwd(h, w, target, dloss, loss, lse, dh, dw, S, Dm, V, seq_tile, 0, 0, stream)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    upipe_ce_fwd_bwd(h, w, target, dloss, loss, lse, dh, dw, S, Dm, V, seq_tile, workspace, None,
+                     stream)
+    return loss, lse, dh, dw
 
 
 def mlp_forward(x, w_gu, w_d, seq_tile=8192, workspace=None, stream=None, y_on_host=False):

@@ -19,7 +19,8 @@
 // Epilogues (the per-token loss, "Road to 5 million sequence length" talk notes, Arctic
 // sequence-tiling passage; "Road to 5 Million Tokens" summary, section 2 item 5):
 //   CE_FWD    logits -> per (row, 256-column tile): running max (log2 units) and sum of
-//             2^(x log2e - max); the logit at the row's target when it falls in the tile
+//             2^(x log2e - max); the logit at the row's target when it falls in the tile;
+//             optionally the fp32 logits themselves (the fused forward + backward)
 //   CE_BWD    logits -> dlogits = g_row * (exp(logit - lse_row) - [col == target]) as bf16
 //   STORE     C -> bf16
 //   ACC_F32   C -> fp32, added to what is there when accumulating, else stored
@@ -100,7 +101,13 @@ struct Epi<kEpiCeFwd> {
     tl = 0.f;
     tg = row_ok ? a.target[row] : -1;
   }
-  __device__ void slice(const GemmArgs&, int64_t, bool, int col0, const float* x) {
+  __device__ void slice(const GemmArgs& a, int64_t row, bool row_ok, int col0, const float* x) {
+    if (a.c && row_ok) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.c) + row * a.ldc + col0);
+#pragma unroll
+      for (int v = 0; v < 8; ++v)
+        dst[v] = make_float4(x[4 * v], x[4 * v + 1], x[4 * v + 2], x[4 * v + 3]);
+    }
     float cm = x[0];
 #pragma unroll
     for (int j = 1; j < 32; ++j) cm = fmaxf(cm, x[j]);
@@ -453,15 +460,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t rg[32], ru[32];
           tmem_ld32_sync(tD + static_cast<uint32_t>(c), rg);
           tmem_ld32_sync(tD + static_cast<uint32_t>(kOut + c), ru);
-          e.slice2(a, row, row_ok, n0 + c, reinterpret_cast<const float*>(rg),
-                   reinterpret_cast<const float*>(ru));
+          float xg[32], xu[32];  // explicit bit casts: no float access through the uint32 array
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            xg[j] = __uint_as_float(rg[j]);
+            xu[j] = __uint_as_float(ru[j]);
+          }
+          e.slice2(a, row, row_ok, n0 + c, xg, xu);
         }
       } else {
         for (int c = 0; c < kBN; c += 32) {
           if (n0 + c >= a.N) break;  // N % 64 == 0: a slice is wholly inside or outside
           uint32_t r[32];
           tmem_ld32_sync(tD + static_cast<uint32_t>(c), r);
-          e.slice(a, row, row_ok, n0 + c, reinterpret_cast<const float*>(r));
+          float x[32];  // explicit bit casts: no float access through the uint32 array
+#pragma unroll
+          for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
+          e.slice(a, row, row_ok, n0 + c, x);
         }
       }
       e.end(a, row, row_ok, nt, n0);
@@ -501,6 +516,33 @@ __global__ void ce_merge_kernel(const float2* __restrict__ part, int64_t part_st
   loss[row] = tg < 0 ? 0.f : (tg < V ? l - tlogit[row] : __int_as_float(0x7fc00000));
 }
 
+// One block per token row: dl[r][j] = g_r (exp(L[r][j] - lse_r) - [j == target_r]) as bf16,
+// from the fp32 logits the CE_FWD epilogue stored - the same arithmetic, in the same order, as
+// the CE_BWD epilogue applies to recomputed logits, so both give the same bits. Rows of ignored
+// tokens are zero; a target outside the vocabulary makes its row NaN. V % 8 == 0.
+__global__ void ce_dlogits_kernel(const float* __restrict__ L, const float* __restrict__ lse,
+                                  const int64_t* __restrict__ target, const float* __restrict__ g,
+                                  __nv_bfloat16* __restrict__ dl, int64_t V) {
+  const int64_t r = blockIdx.x;
+  const int64_t tg = target[r];
+  float gi = tg >= 0 ? g[r] : 0.f;
+  if (tg >= V) gi = __int_as_float(0x7fc00000);
+  const float lse2 = lse[r] * kLog2e;
+  const float4* src = reinterpret_cast<const float4*>(L + r * V);
+  uint4* dst = reinterpret_cast<uint4*>(dl + r * V);
+  for (int64_t q = threadIdx.x; q < V / 8; q += blockDim.x) {
+    const float4 u = src[2 * q], w = src[2 * q + 1];
+    const float x[8] = {u.x, u.y, u.z, u.w, w.x, w.y, w.z, w.w};
+    float d[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float p = ex2_approx(fmaf(x[k], kLog2e, -lse2));
+      d[k] = gi * (p - (8 * q + k == tg ? 1.f : 0.f));
+    }
+    dst[q] = pack8(d);
+  }
+}
+
 template <int EPI, bool A_MN, bool B_MN>
 cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
                        int grid_cap, cudaStream_t stream) {
@@ -536,6 +578,17 @@ cudaError_t launch_gemm_tc(int epi, bool a_mn, bool b_mn, const CUtensorMap& ta,
   if (epi == kEpiSwiglu && !a_mn && !b_mn) return launch_one<kEpiSwiglu, false, false>(ta, tb, a, grid_cap, stream);
   if (epi == kEpiDSwiglu && !a_mn && b_mn) return launch_one<kEpiDSwiglu, false, true>(ta, tb, a, grid_cap, stream);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_ce_dlogits(const float* logits, const float* lse, const int64_t* target,
+                              const float* g, void* dl, int64_t M, int64_t V, cudaStream_t stream) {
+  if (M <= 0) return cudaSuccess;
+  launch_begin(7, stream);
+  ce_dlogits_kernel<<<static_cast<unsigned>(M), 256, 0, stream>>>(
+      logits, lse, target, g, static_cast<__nv_bfloat16*>(dl), V);
+  cudaError_t e = cudaGetLastError();
+  launch_end(7, stream);
+  return e;
 }
 
 cudaError_t launch_ce_merge(const float* part, int64_t part_stride, int n_parts,

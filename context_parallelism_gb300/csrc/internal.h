@@ -124,7 +124,8 @@ struct GemmArgs {
   int M, N, K;            // N % 64 == 0; M, K any (tensor maps zero-fill past the edges)
   int m_fastest;          // tile order: 1 walks M tiles first (shares a B strip), 0 N tiles first
   int group_m;            // tiles of the fast dimension per group (<= 0: all), see tile_coords
-  void* c;                // STORE: bf16 [M][ldc]; ACC_F32: fp32 [M][ldc]; CE_BWD: bf16 dlogits
+  void* c;                // STORE: bf16 [M][ldc]; ACC_F32: fp32 [M][ldc]; CE_BWD: bf16 dlogits;
+                          // CE_FWD: optional fp32 logits [M][ldc] (NULL: not stored)
   int64_t ldc;
   int accumulate;         // ACC_F32: add into c instead of overwriting
   const int64_t* target;  // CE: [M] vocabulary index of each row's target, < 0 = ignored
@@ -148,6 +149,11 @@ struct GemmArgs {
 cudaError_t launch_gemm_tc(int epi, bool a_mn, bool b_mn, const CUtensorMap& ta,
                            const CUtensorMap& tb, const GemmArgs& a, int grid_cap,
                            cudaStream_t stream);
+
+// dl[r][j] (bf16 [M][V]) = g_r (exp(logits[r][j] - lse_r) - [j == target_r]) from stored fp32
+// logits [M][V]: bitwise what the CE_BWD epilogue gives on recomputed logits.
+cudaError_t launch_ce_dlogits(const float* logits, const float* lse, const int64_t* target,
+                              const float* g, void* dl, int64_t M, int64_t V, cudaStream_t stream);
 
 // loss[r], lse[r] for r < M from the CE_FWD partials of n_parts column tiles (V: vocabulary
 // size, for the out-of-range target check).

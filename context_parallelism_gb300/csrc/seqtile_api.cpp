@@ -263,6 +263,8 @@ struct CePlan {
   int n_vt = 0;       // 256-column vocabulary tiles
   size_t f_part = 0, f_tl = 0, f_h[2] = {0, 0}, f_total = 0;
   size_t b_dl = 0, b_h[2] = {0, 0}, b_dh[2] = {0, 0}, b_total = 0;
+  // fused forward + backward: partials, target logits, fp32 logits, bf16 dlogits
+  size_t x_part = 0, x_tl = 0, x_L = 0, x_dl = 0, x_h[2] = {0, 0}, x_dh[2] = {0, 0}, x_total = 0;
 };
 
 // 0 if the shape is accepted, else a status (message set).
@@ -296,6 +298,20 @@ CePlan make_plan(int64_t S, int Dm, int64_t V, int64_t seq_tile, bool host_act) 
     plan_slots(&off, p.T, row, p.b_dh);
   }
   p.b_total = off;
+  off = 0;
+  p.x_part = off;
+  off += al(static_cast<size_t>(p.n_vt) * p.T_pad * 8);
+  p.x_tl = off;
+  off += al(static_cast<size_t>(p.T_pad) * 4);
+  p.x_L = off;
+  off += al(static_cast<size_t>(p.T) * V * 4);
+  p.x_dl = off;
+  off += al(static_cast<size_t>(p.T) * V * 2);
+  if (host_act) {
+    plan_slots(&off, p.T, row, p.x_h);
+    plan_slots(&off, p.T, row, p.x_dh);
+  }
+  p.x_total = off;
   return p;
 }
 
@@ -381,11 +397,12 @@ extern "C" {
 size_t upipe_ce_workspace_bytes(int64_t S, int Dm, int64_t V, int64_t seq_tile, int pass,
                                 int host_mask) {
   if (check_shape(S, Dm, V, seq_tile) != UPIPE_OK) return 0;
-  if (pass < UPIPE_PASS_FWD || pass > UPIPE_PASS_BOTH) return 0;
+  if (pass < UPIPE_PASS_FWD || pass > UPIPE_PASS_FUSED) return 0;
   if (host_mask & ~UPIPE_HOST_ACT) return 0;
   const CePlan p = make_plan(S, Dm, V, seq_tile, (host_mask & UPIPE_HOST_ACT) != 0);
   if (pass == UPIPE_PASS_FWD) return p.f_total;
   if (pass == UPIPE_PASS_BWD) return p.b_total;
+  if (pass == UPIPE_PASS_FUSED) return p.x_total;
   return p.f_total > p.b_total ? p.f_total : p.b_total;
 }
 
@@ -507,6 +524,93 @@ int upipe_ce_bwd(const void* h, const void* w, const int64_t* target, const floa
     LOSS_CUDA(launch_gemm_tc(kEpiStoreBf16, false, true, tdl_k, tw_mn, x, cap, stream));
 
     GemmArgs y{};
+    y.M = static_cast<int>(V);
+    y.N = Dm;
+    y.K = static_cast<int>(Mc);
+    y.m_fastest = 0;
+    y.group_m = UPIPE_WG_GROUP_N;
+    y.c = dw;
+    y.ldc = Dm;
+    y.accumulate = r0 > 0 ? 1 : 0;
+    y.err = err;
+    LOSS_CUDA(launch_gemm_tc(kEpiAccF32, true, true, tdl_mn, th_mn, y, cap, stream));
+    return UPIPE_OK;
+  });
+}
+
+int upipe_ce_fwd_bwd(const void* h, const void* w, const int64_t* target, const float* dloss,
+                     float* loss, float* lse, void* dh, float* dw, int64_t S, int Dm, int64_t V,
+                     int64_t seq_tile, void* workspace, size_t workspace_bytes, void* stream_) {
+  set_last_error("");
+  int st = check_shape(S, Dm, V, seq_tile);
+  if (st != UPIPE_OK) return st;
+  const void* ptrs[9] = {h, w, target, dloss, loss, lse, dh, dw, workspace};
+  const char* names[9] = {"h", "w", "target", "dloss", "loss", "lse", "dh", "dw", "workspace"};
+  const bool may_host[9] = {true, false, false, false, false, false, true, false, false};
+  bool host[9];
+  int dev = -1;
+  st = check_ptrs(ptrs, names, may_host, 9, host, &dev);
+  if (st != UPIPE_OK) return st;
+  const CePlan p = make_plan(S, Dm, V, seq_tile, host[0] || host[6]);
+  if (workspace_bytes < p.x_total)
+    return lfail(UPIPE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes,
+                 p.x_total);
+  LOSS_CUDA(cudaSetDevice(dev));
+  uint32_t* err = nullptr;
+  st = device_status_word(dev, &err);
+  if (st != UPIPE_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* part = reinterpret_cast<float*>(ws + p.x_part);
+  float* tl = reinterpret_cast<float*>(ws + p.x_tl);
+  float* logits = reinterpret_cast<float*>(ws + p.x_L);
+  void* dl = ws + p.x_dl;
+  const int cap = sm_count(dev);
+
+  const Act in[1] = {make_act(h, int64_t(Dm) * 2, host[0], ws, p.x_h)};
+  const Act out[1] = {make_act(dh, int64_t(Dm) * 2, host[6], ws, p.x_dh)};
+  CUtensorMap tw_k, tw_mn;
+  LOSS_CUDA(make_tmap_bf16(&tw_k, w, Dm, V, 1, 256));   // w as B [N = V][K = Dm]
+  LOSS_CUDA(make_tmap_bf16(&tw_mn, w, Dm, V, 1, 64));   // w as B [K = V][N = Dm]
+  return run_tiles(S, p.T, in, 1, out, 1, dev, stream,
+                   [&](int64_t r0, int64_t Mc, int s) -> int {
+    const uint8_t* hc = in[0].rows(s, r0);
+    CUtensorMap th_k, th_mn, tdl_k, tdl_mn;
+    LOSS_CUDA(make_tmap_bf16(&th_k, hc, Dm, Mc, 1, 128));
+    LOSS_CUDA(make_tmap_bf16(&th_mn, hc, Dm, Mc, 1, 64));
+    LOSS_CUDA(make_tmap_bf16(&tdl_k, dl, V, Mc, 1, 128));
+    LOSS_CUDA(make_tmap_bf16(&tdl_mn, dl, V, Mc, 1, 64));
+
+    GemmArgs a{};  // logits: loss statistics, and the fp32 logits kept for the backward
+    a.M = static_cast<int>(Mc);
+    a.N = static_cast<int>(V);
+    a.K = Dm;
+    a.m_fastest = 1;
+    a.group_m = UPIPE_CE_GROUP_M;
+    a.c = logits;
+    a.ldc = V;
+    a.target = target + r0;
+    a.part = part;
+    a.part_stride = p.T_pad;
+    a.tlogit = tl;
+    a.err = err;
+    LOSS_CUDA(launch_gemm_tc(kEpiCeFwd, false, false, th_k, tw_k, a, cap, stream));
+    LOSS_CUDA(launch_ce_merge(part, p.T_pad, p.n_vt, tl, target + r0, loss + r0, lse + r0, Mc,
+                              V, stream));
+    LOSS_CUDA(launch_ce_dlogits(logits, lse + r0, target + r0, dloss + r0, dl, Mc, V, stream));
+
+    GemmArgs x{};  // dh = dlogits w
+    x.M = static_cast<int>(Mc);
+    x.N = Dm;
+    x.K = static_cast<int>(V);
+    x.m_fastest = 0;
+    x.group_m = UPIPE_ST_GROUP_N;
+    x.c = out[0].rows(s, r0);
+    x.ldc = Dm;
+    x.err = err;
+    LOSS_CUDA(launch_gemm_tc(kEpiStoreBf16, false, true, tdl_k, tw_mn, x, cap, stream));
+
+    GemmArgs y{};  // dw += dlogits^T h
     y.M = static_cast<int>(V);
     y.N = Dm;
     y.K = static_cast<int>(Mc);

@@ -59,8 +59,9 @@ typedef enum {
   UPIPE_ERR_TIMEOUT = 5               /* a kernel's bounded wait expired (see sync_status) */
 } upipe_status;
 
-/* Which pass a workspace is sized for. */
-enum { UPIPE_PASS_FWD = 0, UPIPE_PASS_BWD = 1, UPIPE_PASS_BOTH = 2 };
+/* Which pass a workspace is sized for. UPIPE_PASS_FUSED: the loss's one-call forward and
+ * backward (upipe_ce_fwd_bwd); every other workspace query returns 0 for it. */
+enum { UPIPE_PASS_FWD = 0, UPIPE_PASS_BWD = 1, UPIPE_PASS_BOTH = 2, UPIPE_PASS_FUSED = 3 };
 
 /* What may live in pinned host memory (bits of upipe_workspace_bytes' host_mask):
  * UPIPE_HOST_KV: k and v (and then dk, dv); UPIPE_HOST_ACT: q and o in the forward, q, o, dout
@@ -228,6 +229,17 @@ int upipe_ce_fwd(const void* h, const void* w, const int64_t* target, float* los
 int upipe_ce_bwd(const void* h, const void* w, const int64_t* target, const float* lse,
                  const float* dloss, void* dh, float* dw, int64_t S, int Dm, int64_t V,
                  int64_t seq_tile, void* workspace, size_t workspace_bytes, void* stream);
+/* Forward and backward in one call, for an upstream gradient dloss known up front (the loss
+ * is the last operation: dloss = 1/count for a mean). Per tile the logits GEMM also keeps its
+ * fp32 logits (seq_tile x V x 4 bytes of workspace) and one HBM-bound pass turns them into
+ * dlogits after the merge, so the backward's logits recompute - a quarter of the two calls'
+ * tensor work - is not done. loss, lse, dh and dw are bitwise those of upipe_ce_fwd followed
+ * by upipe_ce_bwd. Workspace: upipe_ce_workspace_bytes(..., UPIPE_PASS_FUSED, host_mask) =
+ * the forward's partials + T*V*4 (logits) + T*V*2 (dlogits) bytes, T = min(seq_tile, S),
+ * each rounded up to 256, plus 4 staging slots with UPIPE_HOST_ACT (h in, dh out). */
+int upipe_ce_fwd_bwd(const void* h, const void* w, const int64_t* target, const float* dloss,
+                     float* loss, float* lse, void* dh, float* dw, int64_t S, int Dm, int64_t V,
+                     int64_t seq_tile, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---- Sequence tiling: gated (SwiGLU) MLP ------------------------------------------------
  *
@@ -272,7 +284,7 @@ enum {
   UPIPE_K_DQ_CONVERT = 4, /* dq float32 -> bf16 token-major */
   UPIPE_K_OTHER = 5,      /* self-tests */
   UPIPE_K_LOSS_GEMM = 6,  /* sequence-tiled loss and MLP: tensor-core GEMMs + epilogues */
-  UPIPE_K_LOSS_MERGE = 7, /* sequence-tiled loss: per-token merge of the vocabulary tiles */
+  UPIPE_K_LOSS_MERGE = 7, /* sequence-tiled loss: per-token merge, stored logits -> dlogits */
   UPIPE_K_COUNT = 8
 };
 

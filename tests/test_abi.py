@@ -264,3 +264,18 @@ def test_copy_failure_hook_arms_and_validates_without_gpu():
     assert up._lib.upipe_debug_fail_copy_after(-1) == up.UPIPE_ERR_INVALID_ARG
     up.upipe_debug_fail_copy_after(5)
     up.upipe_debug_fail_copy_after(0)  # disarmed again
+
+
+@pytest.mark.parametrize("S,Dm,V,T", [(131072, 4096, 128256, 8192), (1000, 256, 1088, 256)])
+def test_fused_loss_workspace_matches_formula(S, Dm, V, T):
+    al = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    Tt = min(T, S)
+    Tp = (Tt + 127) // 128 * 128
+    fused = al((V + 255) // 256 * Tp * 8) + al(Tp * 4) + al(Tt * V * 4) + al(Tt * V * 2)
+    assert up.upipe_ce_workspace_bytes(S, Dm, V, T, up.UPIPE_PASS_FUSED) == fused
+    slot = al(Tt * Dm * 2)
+    assert up.upipe_ce_workspace_bytes(S, Dm, V, T, up.UPIPE_PASS_FUSED, up.UPIPE_HOST_ACT) == \
+        fused + 4 * slot
+    # the attention and MLP workspaces have no fused pass
+    assert up.upipe_workspace_bytes(1, 1024, 8, 2, 128, 1, 4, 1024, up.UPIPE_PASS_FUSED) == 0
+    assert up.upipe_mlp_workspace_bytes(S, Dm, 128, T, up.UPIPE_PASS_FUSED) == 0

@@ -133,6 +133,47 @@ def test_host_activations_equal_device(S, T):
     assert torch.equal(dh, ref[2].cpu()) and torch.equal(dw, ref[3])
 
 
+@pytest.mark.parametrize("S,Dm,V,T,host", [(1000, 256, 1088, 256, False),
+                                           (300, 64, 320, 128, False),
+                                           (1000, 256, 1088, 256, True),
+                                           (1, 64, 256, 128, False)])
+def test_fused_forward_backward_equals_two_calls(S, Dm, V, T, host):
+    """upipe_ce_fwd_bwd keeps the forward's fp32 logits instead of recomputing them: loss, lse,
+    dh and dw are bitwise those of the two calls (and so within tolerance of the oracle)."""
+    lw = LOSS_WORKLOADS["readout_small"].with_(S=S, Dm=Dm, V=V, seed=81 + S + V)
+    h, w, t, _ = make_loss_inputs(lw, "cpu")
+    g = _random_g(S, lw.seed)
+    ref = _run(h, w, t, g, T)
+    hi = h.cuda()
+    if host:
+        hi = torch.empty(h.shape, dtype=h.dtype, pin_memory=True)
+        hi.copy_(h)
+    got = up.ce_loss_fused(hi, w.cuda(), t.cuda(), g.cuda(), seq_tile=T, dh_on_host=host)
+    up.upipe_sync_status()
+    for a, b in zip(got, ref):
+        assert torch.equal(a.cpu(), b.cpu())
+    rl, rs, rdh, rdw = oracle.ce_loss_bwd_ref(h, w, t, g)
+    assert max_abs(to_np(got[0]), rl) <= LOSS_MAX_ABS
+    assert rel_fro(to_np(got[2]), rdh) <= GRAD_REL_FRO and rel_fro(to_np(got[3]), rdw) <= GRAD_REL_FRO
+
+
+def test_fused_at_width_4096_and_full_vocabulary():
+    """The measured shape's width and vocabulary over two 8192-token tiles: bitwise the two
+    calls, and sampled tokens against the oracle."""
+    lw = LOSS_WORKLOADS["llama8b_readout_s128k"].with_(S=16384)
+    h, w, t, g = make_loss_inputs(lw)
+    loss, lse = up.ce_loss_forward(h, w, t, seq_tile=8192)
+    dh, dw = up.ce_loss_backward(h, w, t, lse, g, seq_tile=8192)
+    got = up.ce_loss_fused(h, w, t, g, seq_tile=8192)
+    up.upipe_sync_status()
+    assert torch.equal(got[0], loss) and torch.equal(got[1], lse)
+    assert torch.equal(got[2], dh) and torch.equal(got[3], dw)
+    rows = [0, 8191, 8192, 16383]
+    rl, rs, rdh = oracle.ce_rows_ref(h, w, t, g, rows)
+    assert max_abs(to_np(got[0][rows]), rl) <= LOSS_MAX_ABS
+    assert rel_fro(to_np(got[2][rows]), rdh) <= GRAD_REL_FRO
+
+
 @pytest.mark.slow
 def test_loss_full_size_sampled():
     """The measured configuration (S = 128K tokens, Dm 4096, V 128256, tiles of 8192) in the
