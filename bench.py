@@ -89,13 +89,13 @@ TRAFFIC = {
         {"workload": "llama8b_readout_s128k", "head_chunk": 8192, "seq_trunk": None,
          "files": ["context_parallelism_gb300/csrc/gemm_tc.cu",
                    "context_parallelism_gb300/csrc/seqtile_api.cpp"],
-         "sha256": "1c2aafc93fc6c36438f0cc82aa80e78d9c57194496da00888c54cb92cdf445ab",
-         "bytes": 5913879764},
+         "sha256": "28c165205bf6f97b0b9d7b9d663d8761634e7e605ef794e201d64d09fd1b02f8",
+         "bytes": 5916616972},
         {"workload": "llama8b_mlp_s128k", "head_chunk": 8192, "seq_trunk": None,
          "files": ["context_parallelism_gb300/csrc/gemm_tc.cu",
                    "context_parallelism_gb300/csrc/seqtile_api.cpp"],
-         "sha256": "1c2aafc93fc6c36438f0cc82aa80e78d9c57194496da00888c54cb92cdf445ab",
-         "bytes": 1350233074},
+         "sha256": "28c165205bf6f97b0b9d7b9d663d8761634e7e605ef794e201d64d09fd1b02f8",
+         "bytes": 1364604509},
     ],
 }
 
