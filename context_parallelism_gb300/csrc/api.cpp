@@ -488,6 +488,7 @@ size_t upipe_workspace_bytes(int B, int64_t S, int Hq, int Hkv, int D, int causa
 int upipe_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                    int64_t S, int Hq, int Hkv, int D, int causal, int head_chunk,
                    int64_t seq_trunk, void* workspace, size_t workspace_bytes, void* stream_) {
+  const NvtxRange range("upipe_attn_fwd");
   g_last_error.clear();
   // lse may be NULL: a prefill (inference) forward that keeps no statistics for a backward
   if (!q || !k || !v || !o || !workspace)
@@ -594,6 +595,7 @@ int upipe_attn_fwd(const void* q, const void* k, const void* v, void* o, float* 
   };
   int job = 0;
   for (int g = 0; g < n_groups; ++g) {
+    const NvtxRange range("upipe fwd head group %lld", g);
     const int h0 = g * p.hc, kvh0 = g * p.kc;
     const int gs = g & 1;
     uint8_t* qwg = q_buf(g);
@@ -671,6 +673,7 @@ int upipe_attn_bwd(const void* q, const void* k, const void* v, const void* o, c
                    const void* dout, void* dq, void* dk, void* dv, int B, int64_t S, int Hq,
                    int Hkv, int D, int causal, int head_chunk, int64_t seq_trunk,
                    void* workspace, size_t workspace_bytes, void* stream_) {
+  const NvtxRange range("upipe_attn_bwd");
   g_last_error.clear();
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace)
     return fail(UPIPE_ERR_INVALID_ARG, "null pointer argument");
@@ -779,6 +782,7 @@ int upipe_attn_bwd(const void* q, const void* k, const void* v, const void* o, c
   }
   int job = 0;
   for (int g = 0; g < n_groups; ++g) {
+    const NvtxRange range("upipe bwd head group %lld", g);
     const int h0 = g * p.hc, kvh0 = g * p.kc;
     const int gs = g & 1;
     void* qw = qw_of(g);

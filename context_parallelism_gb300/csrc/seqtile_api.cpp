@@ -205,7 +205,10 @@ int run_tiles(int64_t S, int64_t T, const Act* ins, int n_in, const Act* outs, i
     if (any_in) LOSS_CUDA(cudaStreamWaitEvent(stream, sg->in_ready[s], 0));
     // the slot's outputs from tile i - 2 must have left before this tile overwrites them
     if (any_out && i >= 2) LOSS_CUDA(cudaStreamWaitEvent(stream, sg->out_free[s], 0));
-    if ((st = body(r0, Mc, s)) != UPIPE_OK) return st;
+    {
+      const NvtxRange range("upipe tile %lld", static_cast<long long>(i));
+      if ((st = body(r0, Mc, s)) != UPIPE_OK) return st;
+    }
     if (any_in) {
       LOSS_CUDA(cudaEventRecord(sg->in_free[s], stream));
       if (i + 2 < n_tiles && (st = issue_in(i + 2)) != UPIPE_OK) return st;
@@ -409,6 +412,7 @@ size_t upipe_ce_workspace_bytes(int64_t S, int Dm, int64_t V, int64_t seq_tile, 
 int upipe_ce_fwd(const void* h, const void* w, const int64_t* target, float* loss, float* lse,
                  int64_t S, int Dm, int64_t V, int64_t seq_tile, void* workspace,
                  size_t workspace_bytes, void* stream_) {
+  const NvtxRange range("upipe_ce_fwd");
   set_last_error("");
   int st = check_shape(S, Dm, V, seq_tile);
   if (st != UPIPE_OK) return st;
@@ -461,6 +465,7 @@ int upipe_ce_fwd(const void* h, const void* w, const int64_t* target, float* los
 int upipe_ce_bwd(const void* h, const void* w, const int64_t* target, const float* lse,
                  const float* dloss, void* dh, float* dw, int64_t S, int Dm, int64_t V,
                  int64_t seq_tile, void* workspace, size_t workspace_bytes, void* stream_) {
+  const NvtxRange range("upipe_ce_bwd");
   set_last_error("");
   int st = check_shape(S, Dm, V, seq_tile);
   if (st != UPIPE_OK) return st;
@@ -541,6 +546,7 @@ int upipe_ce_bwd(const void* h, const void* w, const int64_t* target, const floa
 int upipe_ce_fwd_bwd(const void* h, const void* w, const int64_t* target, const float* dloss,
                      float* loss, float* lse, void* dh, float* dw, int64_t S, int Dm, int64_t V,
                      int64_t seq_tile, void* workspace, size_t workspace_bytes, void* stream_) {
+  const NvtxRange range("upipe_ce_fwd_bwd");
   set_last_error("");
   int st = check_shape(S, Dm, V, seq_tile);
   if (st != UPIPE_OK) return st;
@@ -641,6 +647,7 @@ size_t upipe_mlp_workspace_bytes(int64_t S, int Dm, int F, int64_t seq_tile, int
 int upipe_mlp_fwd(const void* x, const void* w_gu, const void* w_d, void* y, int64_t S, int Dm,
                   int F, int64_t seq_tile, void* workspace, size_t workspace_bytes,
                   void* stream_) {
+  const NvtxRange range("upipe_mlp_fwd");
   set_last_error("");
   int st = check_mlp_shape(S, Dm, F, seq_tile);
   if (st != UPIPE_OK) return st;
@@ -702,6 +709,7 @@ int upipe_mlp_fwd(const void* x, const void* w_gu, const void* w_d, void* y, int
 int upipe_mlp_bwd(const void* x, const void* w_gu, const void* w_d, const void* dy, void* dx,
                   float* dw_gu, float* dw_d, int64_t S, int Dm, int F, int64_t seq_tile,
                   void* workspace, size_t workspace_bytes, void* stream_) {
+  const NvtxRange range("upipe_mlp_bwd");
   set_last_error("");
   int st = check_mlp_shape(S, Dm, F, seq_tile);
   if (st != UPIPE_OK) return st;
