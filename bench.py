@@ -89,13 +89,13 @@ TRAFFIC = {
         {"workload": "llama8b_readout_s128k", "head_chunk": 8192, "seq_trunk": None,
          "files": ["context_parallelism_gb300/csrc/gemm_tc.cu",
                    "context_parallelism_gb300/csrc/seqtile_api.cpp"],
-         "sha256": "28c165205bf6f97b0b9d7b9d663d8761634e7e605ef794e201d64d09fd1b02f8",
-         "bytes": 5916616972},
+         "sha256": "b112e92702e28c192d3ce6c51c282e2f3308cedf620d5209a1dae5ce2e8406a8",
+         "bytes": 5925529448},
         {"workload": "llama8b_mlp_s128k", "head_chunk": 8192, "seq_trunk": None,
          "files": ["context_parallelism_gb300/csrc/gemm_tc.cu",
                    "context_parallelism_gb300/csrc/seqtile_api.cpp"],
-         "sha256": "28c165205bf6f97b0b9d7b9d663d8761634e7e605ef794e201d64d09fd1b02f8",
-         "bytes": 1364604509},
+         "sha256": "b112e92702e28c192d3ce6c51c282e2f3308cedf620d5209a1dae5ce2e8406a8",
+         "bytes": 1366615122},
     ],
 }
 
