@@ -50,6 +50,10 @@ def _args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-explicit-copies", action="store_true",
+                    help="tiled workloads: measure e2e through the library's host staging only "
+                         "(skips the user-copy variant and its second set of pinned buffers, "
+                         "for sequences whose activations would not fit host memory twice)")
     ap.add_argument("--seq-len", type=int, default=None,
                     help="override S (small profiling captures only; not a bench line)")
     ap.add_argument("--sweep", default=None, choices=["chunk-trunk", "host-kv"],
@@ -877,7 +881,7 @@ def run_tiled(a, make_spec):
         "roofline": roofline, "kernels": kernels, "gpu_launches": int(launches), "clocks": clk,
         **extra_measured,
     }
-    if not a.no_e2e:
+    if not a.no_e2e and not a.no_explicit_copies:
         # host buffers in (every input), every output out, each step
         ins, outs_d = sp["inputs"], sp["outputs"]
         hh = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in ins]
@@ -909,6 +913,9 @@ def run_tiled(a, make_spec):
                               "and every output copied out, on the compute stream, around "
                               "device-buffer calls"}
         del hh, outs
+    else:
+        explicit = None
+    if not a.no_e2e:
         # the step through the library with the activations in pinned host memory
         host_step, h2d, d2h, wb, method = sp["host_setup"]()
         host_step()
