@@ -30,9 +30,10 @@
  *   - `stream` is a cudaStream_t (NULL = legacy default stream). All work is enqueued on it
  *     and calls return before the GPU finishes (asynchronous, like a kernel launch).
  *   - Devices: one process drives one GPU (one process per GPU under torchrun). Each kernel's
- *     shared-memory size attribute is set once per process, on the device of the first call;
- *     a process that calls the library on a second GPU gets UPIPE_ERR_CUDA from launches that
- *     need more than 48 KiB of shared memory there (no fault).
+ *     shared-memory size attribute is set once per process, on the device of the first call.
+ *     Calling the library on a second GPU from the same process is untested: where the
+ *     attribute does not carry over, launches needing more than 48 KiB of shared memory fail
+ *     there with UPIPE_ERR_CUDA (an error, not a fault).
  *   - Ownership: the caller owns every buffer, including the workspace. Per call the library
  *     allocates no device memory. Per device it lazily creates two internal copy streams for
  *     the attention calls and two for the sequence-tiled calls (used only when activations
