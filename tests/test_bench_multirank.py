@@ -48,3 +48,23 @@ def test_two_gloo_ranks_take_the_slowest_time():
     for rank, tf, t_max in res:
         assert t_max == 1000.0
         assert tf == pytest.approx(2 * 5 * 1e12 / 1.0 / 1e12)
+
+
+def test_traffic_lookup_matches_workload_schedule_and_source_hash(monkeypatch):
+    import bench
+    # the recorded entries apply to their own workload and schedule only
+    assert bench.traffic_per_launch("attn_bwd", "llama8b_s8k", 8, 131072) is None
+    assert bench.traffic_per_launch("attn_bwd", "llama8b_s128k", 16, 131072) is None
+    assert bench.traffic_per_launch("no_such_kernel", "llama8b_s128k", 8, 131072) is None
+    # a source change makes every figure taken on the old source unusable (null)
+    monkeypatch.setattr(bench, "source_hash", lambda files: "0" * 64)
+    assert bench.traffic_per_launch("attn_bwd", "llama8b_s128k", 8, 131072) is None
+    assert bench.traffic_per_launch("loss_gemm", "llama8b_readout_s128k", 8192, None) is None
+    # with the recorded hash each entry is found, one per workload for a shared kernel class
+    monkeypatch.setattr(bench, "source_hash",
+                        lambda files: next(e["sha256"] for es in bench.TRAFFIC.values()
+                                           for e in (es if isinstance(es, list) else [es])
+                                           if e["files"] == files))
+    a = bench.traffic_per_launch("loss_gemm", "llama8b_readout_s128k", 8192, None)
+    b = bench.traffic_per_launch("loss_gemm", "llama8b_mlp_s128k", 8192, None)
+    assert a and b and a != b
