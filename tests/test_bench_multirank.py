@@ -1,5 +1,6 @@
-"""The benchmark's multi-rank path on CPU: N independent replicas joined only by a MAX
-reduction of their timings over gloo (world size 2), and the whole-job throughput formula."""
+"""Host logic of the benchmark on CPU: the multi-rank path (N independent replicas joined only
+by a MAX reduction of their timings over gloo, world size 2), the whole-job throughput formula,
+and the lookup of recorded DRAM traffic (valid only for its workload, schedule and source)."""
 import os
 import socket
 
