@@ -87,6 +87,16 @@ def _row_stats(logits, tgt):
     return lse, loss
 
 
+def _dlogits(logits, lse, tgt, G):
+    """g (softmax - onehot(target)) for a block of logit rows; rows of ignored tokens are 0."""
+    p = np.exp(logits - lse[:, None])          # softmax rows
+    valid = tgt >= 0
+    rows = np.nonzero(valid)[0]
+    p[rows, tgt[rows]] -= 1.0
+    p *= np.where(valid, G, 0.0)[:, None]
+    return p
+
+
 def ce_loss_ref(h, w, target, block: int = 512):
     """Forward: per-token (loss, lse), each float64 [S]."""
     H, W, t = _f64(h), _f64(w), _i64(target)
@@ -112,11 +122,7 @@ def ce_loss_bwd_ref(h, w, target, g, block: int = 512):
         logits = H[r0:r1] @ W.T
         tb = t[r0:r1]
         lse[r0:r1], loss[r0:r1] = _row_stats(logits, tb)
-        p = np.exp(logits - lse[r0:r1, None])          # softmax rows
-        valid = tb >= 0
-        rows = np.nonzero(valid)[0]
-        p[rows, tb[rows]] -= 1.0
-        p *= np.where(valid, G[r0:r1], 0.0)[:, None]    # dlogits
+        p = _dlogits(logits, lse[r0:r1], tb, G[r0:r1])
         dh[r0:r1] = p @ W
         dw += p.T @ H[r0:r1]
     return loss, lse, dh, dw
@@ -139,11 +145,7 @@ def ce_rows_ref(h, w, target, g, rows, vocab_rows=None):
     W = _f64(w)
     logits = H @ W.T
     lse, loss = _row_stats(logits, t)
-    p = np.exp(logits - lse[:, None])
-    valid = t >= 0
-    vr = np.nonzero(valid)[0]
-    p[vr, t[vr]] -= 1.0
-    p *= np.where(valid, G, 0.0)[:, None]
+    p = _dlogits(logits, lse, t, G)
     if vocab_rows is None:
         return loss, lse, p @ W
     vr = np.asarray(vocab_rows, dtype=np.int64)
