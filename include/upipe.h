@@ -39,10 +39,13 @@
  *     the attention calls and two for the sequence-tiled calls (used only when activations
  *     are pinned host memory), a few events and a 256-byte device status word;
  *     upipe_shutdown() releases them.
- *   - Errors: all arguments are validated before anything is enqueued; on an error nothing
- *     is launched and a status code is returned (see upipe_status). A device-side bounded
- *     wait that expires sets the device status word and the kernel exits early; the host
- *     learns of it through upipe_sync_status(). Asynchronous CUDA faults surface at the
+ *   - Errors: all arguments are validated before anything is enqueued; on an argument error
+ *     nothing is launched and a status code is returned (see upipe_status). A CUDA call that
+ *     fails part-way through a call (UPIPE_ERR_CUDA) returns at once: work already enqueued,
+ *     including copies on the library's copy streams, still runs, so synchronise the device
+ *     before reusing or freeing that call's buffers; its outputs are undefined. A device-side
+ *     bounded wait that expires sets the device status word and the kernel exits early; the
+ *     host learns of it through upipe_sync_status(). Asynchronous CUDA faults surface at the
  *     caller's next synchronisation.
  */
 #ifndef UPIPE_H_
