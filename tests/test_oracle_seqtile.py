@@ -262,3 +262,31 @@ def test_mlp_rows_and_blocking_agree_with_whole_problem():
     _, _, dwg, dwd = mlp_rows_ref(x, w_gu, w_d, dys, rows, gu_rows=gr, d_rows=dr)
     assert np.allclose(dwg, dwg_full[gr], rtol=0, atol=1e-12)
     assert np.allclose(dwd, dwd_full[dr], rtol=0, atol=1e-12)
+
+
+# ---- hand-worked examples (tests/golden/, derivations in each file's "_about") --------------
+
+import json  # noqa: E402
+import os  # noqa: E402
+
+_GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def test_loss_hand_worked_example():
+    e = json.load(open(os.path.join(_GOLDEN, "ce_hand_example_s2_v2.json")))
+    loss, lse, dh, dw = ce_loss_bwd_ref(np.array(e["h"]), np.array(e["w"]),
+                                        np.array(e["target"]), np.array(e["g"]))
+    assert np.allclose(loss, e["loss"], rtol=0, atol=1e-14)
+    assert np.allclose(lse, e["lse"], rtol=0, atol=1e-14)
+    assert np.allclose(dh, e["dh"], rtol=0, atol=1e-14)
+    assert np.allclose(dw, e["dw"], rtol=0, atol=1e-14)
+
+
+def test_mlp_hand_worked_example():
+    e = json.load(open(os.path.join(_GOLDEN, "mlp_hand_example_d1_f1.json")))
+    y, dx, dw_gu, dw_d = mlp_bwd_ref(np.array(e["x"]), np.array(e["w_gu"]), np.array(e["w_d"]),
+                                     np.array(e["dy"]))
+    assert np.allclose(y, e["y"], rtol=0, atol=1e-13)
+    assert np.allclose(dx, e["dx"], rtol=0, atol=1e-13)
+    assert np.allclose(dw_gu, e["dw_gu"], rtol=0, atol=1e-13)
+    assert np.allclose(dw_d, e["dw_d"], rtol=0, atol=1e-13)
