@@ -21,7 +21,9 @@ Readings where the pages are silent (all from the workload definitions, not the 
   floor(h / (Hq/Hkv)); LSE uses the natural log and is returned as [B, Hq, S].
 
 Layouts: q, dout, o, dq are token-major [B, S, Hq, D]; k, v, dk, dv are [B, S, Hkv, D].
-All arithmetic is numpy float64; inputs of any float dtype are upcast exactly.
+All arithmetic is float64: numpy, except attn_group_ref, which evaluates the same formulas
+with PyTorch's CPU fp64 operations so that whole slices at S >= 128K use every host core.
+Inputs of any float dtype are upcast exactly.
 
 Parity status: every public function here is pinned by tests/test_oracle.py (finite
 differences, closed forms, invariants, brute force, a library special case).
@@ -37,6 +39,7 @@ __all__ = [
     "attn_bwd_ref",
     "attn_rows_ref",
     "attn_dkdv_window_ref",
+    "attn_group_ref",
     "attn_fwd_trunked_ref",
     "attn_bwd_trunked_ref",
 ]
@@ -219,6 +222,82 @@ def attn_dkdv_window_ref(q, k, v, dout, b, kvh, j0, j1, causal=True, scale=None,
             dk += sc * (dSw.T @ Qb)
             dv += Pw.T @ dOb
     return dk, dv
+
+
+def attn_group_ref(q, k, v, dout, b, kvh, causal=True, scale=None, key_lo=0, key_hi=None,
+                   want_rows=True, row_block=512):
+    """One (batch b, kv-head kvh) slice of the definition, for the full-size checks.
+
+    For every q-head h of the kv-head's group (h in [kvh*G, (kvh+1)*G)):
+      * with want_rows: O_i, LSE_i and dQ_i for every query row i in [row_lo, S);
+      * dK_j and dV_j for key rows j in [key_lo, key_hi) (default: all keys), summed over the
+        group's q-heads and over every query row that sees key j;
+    where row_lo = key_lo when causal (earlier rows see none of the window's keys), else 0.
+    Each row's softmax is taken over its full key range, so every value equals the matching
+    entry of attn_bwd_ref: the same formulas (D_i = <dO_i, O_i>, dS = P (dP - D), dQ, dK,
+    dV as there), evaluated with PyTorch's fp64 CPU operations, whose matrix products and
+    element-wise passes use every host core. That is what makes a whole slice affordable at
+    S = 128K (about 5e13 flops) and a key window at S = 1M.
+
+    Returns (rows [n], o [n, G, D], lse [G, n], dq [n, G, D], dk [m, D], dv [m, D]) as fp64
+    numpy arrays, rows = arange(row_lo, S) (empty arrays when want_rows is False)."""
+    import torch
+
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    G = Hq // Hkv
+    sc = _scale(D, scale)
+    key_hi = S if key_hi is None else int(key_hi)
+    key_lo = int(key_lo)
+    row_lo = key_lo if causal else 0
+    f64 = torch.float64
+
+    def col(x, h, lo=0):  # rows [lo, S) of head h of a [B, S, H, D] tensor, fp64 on the CPU
+        t = torch.as_tensor(x) if not hasattr(x, "detach") else x.detach()
+        return t[b, lo:, h, :].to("cpu").to(f64)
+
+    K = col(k, kvh)
+    V = col(v, kvh)
+    n = S - row_lo if want_rows else 0
+    o = torch.zeros((n, G, D), dtype=f64)
+    lse = torch.zeros((G, n), dtype=f64)
+    dq = torch.zeros((n, G, D), dtype=f64)
+    dk = torch.zeros((key_hi - key_lo, D), dtype=f64)
+    dv = torch.zeros((key_hi - key_lo, D), dtype=f64)
+    for g in range(G):
+        h = kvh * G + g
+        Q = col(q, h, row_lo)
+        dO = col(dout, h, row_lo)
+        for i0 in range(row_lo, S, row_block):
+            i1 = min(S, i0 + row_block)
+            m = i1 if causal else S  # keys past the block's last row are masked for all rows
+            Qb, dOb = Q[i0 - row_lo:i1 - row_lo], dO[i0 - row_lo:i1 - row_lo]
+            s = torch.mm(Qb, K[:m].T).mul_(sc)
+            if causal:  # only columns j >= i0 can lie above a row of this block
+                j = torch.arange(i0, m)[None, :]
+                i = torch.arange(i0, i1)[:, None]
+                s[:, i0:].masked_fill_(j > i, float("-inf"))
+            mx = s.max(dim=1, keepdim=True).values
+            P = s.sub_(mx).exp_()  # in place: s is not needed again
+            l = P.sum(dim=1, keepdim=True)
+            P.div_(l)
+            Ob = P @ V[:m]
+            Di = (dOb * Ob).sum(dim=1, keepdim=True)
+            w1 = min(key_hi, m)
+            if want_rows:
+                dS = torch.mm(dOb, V[:m].T).sub_(Di).mul_(P)
+                r = slice(i0 - row_lo, i1 - row_lo)
+                o[r, g] = Ob
+                lse[g, r] = (mx + torch.log(l))[:, 0]
+                dq[r, g] = sc * (dS @ K[:m])
+                dSw = dS[:, key_lo:w1]
+            else:
+                dSw = torch.mm(dOb, V[key_lo:w1].T).sub_(Di).mul_(P[:, key_lo:w1])
+            if w1 > key_lo:
+                dk[: w1 - key_lo] += sc * (dSw.T @ Qb)
+                dv[: w1 - key_lo] += P[:, key_lo:w1].T @ dOb
+    rows = np.arange(row_lo, S) if want_rows else np.zeros(0, dtype=np.int64)
+    return rows, o.numpy(), lse.numpy(), dq.numpy(), dk.numpy(), dv.numpy()
 
 
 # ----------------------------------------------------------------------------------------

@@ -285,6 +285,64 @@ def test_sampled_rows_and_key_window_match_full(causal):
         np.testing.assert_allclose(wv, dv[0, 50:62, kvh], rtol=0, atol=1e-13)
 
 
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("key_lo,key_hi,want_rows", [(0, None, True), (23, 41, True),
+                                                     (23, 41, False), (60, 70, False)])
+def test_group_slice_matches_full(causal, key_lo, key_hi, want_rows):
+    """attn_group_ref (PyTorch fp64 CPU, for the full-size checks) equals the slice of the
+    pinned numpy oracle: every row of the group's q-heads, every key of the window, with
+    row blocks that do not divide S."""
+    q, k, v, do = random_small(2, 70, 6, 2, 8, 19)
+    o, lse, dq, dk, dv = ref.attn_bwd_ref(q, k, v, do, causal=causal)
+    G = 3
+    for b, kvh in ((0, 1), (1, 0)):
+        rows, go, gl, gdq, gdk, gdv = ref.attn_group_ref(
+            q, k, v, do, b, kvh, causal=causal, key_lo=key_lo, key_hi=key_hi,
+            want_rows=want_rows, row_block=9)
+        hi = 70 if key_hi is None else key_hi
+        np.testing.assert_allclose(gdk, dk[b, key_lo:hi, kvh], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(gdv, dv[b, key_lo:hi, kvh], rtol=0, atol=1e-13)
+        if not want_rows:
+            assert rows.size == 0
+            continue
+        assert rows[0] == (key_lo if causal else 0) and rows[-1] == 69
+        hs = slice(kvh * G, (kvh + 1) * G)
+        np.testing.assert_allclose(go, o[b, rows, hs], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(gl, lse[b, hs][:, rows], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(gdq, dq[b, rows, hs], rtol=0, atol=1e-13)
+
+
+def test_group_slice_closed_form_and_sdpa():
+    """Two pins independent of the numpy oracle: with Q = 0 every causal row is the prefix
+    mean of V, LSE_i = ln(i+1), dK = 0 and dV_j = sum_{i>=j} dO_i/(i+1) summed over the
+    group; on random inputs it equals torch's fp64 scaled_dot_product_attention + autograd."""
+    q, k, v, do = random_small(1, 40, 4, 2, 8, 23)
+    z = torch.zeros_like(q)
+    rows, go, gl, gdq, gdk, gdv = ref.attn_group_ref(z, k, v, do, 0, 1, row_block=7)
+    vv = _np(v)[0, :, 1]
+    dd = _np(do)[0, :, 2:4]
+    n = np.arange(1, 41, dtype=np.float64)
+    prefix = np.cumsum(vv, axis=0) / n[:, None]
+    np.testing.assert_allclose(go[:, 0], prefix, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(go[:, 1], prefix, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(gl, np.log(n)[None, :].repeat(2, 0), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(gdk, 0.0, atol=1e-12)
+    w = (dd / n[:, None, None]).sum(axis=1)
+    want_dv = np.cumsum(w[::-1], axis=0)[::-1]
+    np.testing.assert_allclose(gdv, want_dv, rtol=0, atol=1e-12)
+    qt = q.transpose(1, 2).clone().requires_grad_(True)
+    kt = k.transpose(1, 2).clone().requires_grad_(True)
+    vt = v.transpose(1, 2).clone().requires_grad_(True)
+    ot = torch.nn.functional.scaled_dot_product_attention(
+        qt, kt.repeat_interleave(2, dim=1), vt.repeat_interleave(2, dim=1), is_causal=True)
+    ot.backward(do.transpose(1, 2))
+    rows, go, gl, gdq, gdk, gdv = ref.attn_group_ref(q, k, v, do, 0, 1, row_block=16)
+    np.testing.assert_allclose(go, _np(ot.transpose(1, 2))[0, :, 2:4], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(gdq, _np(qt.grad.transpose(1, 2))[0, :, 2:4], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(gdk, _np(kt.grad.transpose(1, 2))[0, :, 1], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(gdv, _np(vt.grad.transpose(1, 2))[0, :, 1], rtol=0, atol=1e-12)
+
+
 def test_torch_inputs_upcast_exactly():
     q, k, v, do = random_small(1, 16, 2, 1, 8, 1, dtype=torch.bfloat16)
     a = ref.attn_fwd_ref(q, k, v)
