@@ -7,7 +7,8 @@ import torch
 
 import context_parallelism_gb300 as up
 import oracle
-from tests._parity import GRAD_REL_FRO, check_full, gpu_fwd_bwd, pinned_copy, rel_fro, to_np
+from tests._parity import (GRAD_REL_FRO, LSE_MAX_ABS, O_MAX_ABS, check_full, gpu_fwd_bwd,
+                           max_abs, pinned_copy, rel_fro, to_np)
 from workloads import WORKLOADS, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -56,7 +57,10 @@ def test_parity_cases(B, S, Hq, Hkv, D, causal, hc, T, kv_host):
     else:
         kg, vg = k.cuda(), v.cuda()
     gpu = gpu_fwd_bwd(qg, kg, vg, dog, causal, hc, T)
-    check_full(gpu, ref, f"{B}x{S}x{Hq}/{Hkv}x{D} causal={causal} hc={hc} T={T} host={kv_host}")
+    # one token: the exact dQ and dK vanish identically, so their error is held to an
+    # absolute RMS of 1e-3 instead of a relative one
+    check_full(gpu, ref, f"{B}x{S}x{Hq}/{Hkv}x{D} causal={causal} hc={hc} T={T} host={kv_host}",
+               grad_floor_rms=1e-3 if S == 1 else 0.0)
 
 
 def test_head_chunk_does_not_change_forward_bits():
@@ -145,7 +149,8 @@ def test_host_dkdv_needs_host_kv_and_matching_placement():
 @pytest.mark.parametrize("D,host_kv", [(128, False), (128, True), (64, False)])
 def test_prefill_forward_without_lse(D, host_kv):
     """A prefill (inference) forward passes no lse buffer: the same kernels run, only o is
-    written, and it is bitwise the o of the training forward (several trunks, ragged tail)."""
+    written. o matches the fp64 oracle within the forward tolerance, and is bitwise the o of
+    the training forward (several trunks, ragged tail)."""
     w = WORKLOADS["llama8b_s8k"].with_(S=1100, D=D, Hq=8, Hkv=2, seed=38)
     q, k, v, _ = make_inputs(w, "cpu")
     qg = q.cuda()
@@ -154,7 +159,11 @@ def test_prefill_forward_without_lse(D, host_kv):
     o2, l2 = up.attention_forward(qg, kk, vv, causal=True, head_chunk=4, seq_trunk=256,
                                   with_lse=False)
     up.upipe_sync_status()
-    assert l2 is None and torch.equal(o1, o2)
+    assert l2 is None
+    ro, _ = oracle.attn_fwd_ref(q, k, v, causal=True)
+    err = max_abs(to_np(o2), ro)
+    assert err <= O_MAX_ABS, err
+    assert torch.equal(o1, o2)
 
 
 def test_rising_scores_force_rescales():
@@ -182,7 +191,8 @@ def test_rising_scores_force_rescales():
 def test_host_q_and_o_forward(q_host, o_host, kv_host):
     """q read from and o written to pinned host memory, one head group at a time on the copy
     stream (the next group's Q staged and the previous group's O copied out while a group
-    computes): the same kernels, so o and lse are bitwise those of the device-resident run.
+    computes): o and lse match the fp64 oracle, and (the same kernels) are bitwise those of
+    the device-resident run.
     Three head groups exercise both staging buffers and their reuse."""
     w = WORKLOADS["llama8b_s8k"].with_(S=1100, Hq=12, Hkv=3, seed=40)
     q, k, v, _ = make_inputs(w, "cpu")
@@ -194,6 +204,9 @@ def test_host_q_and_o_forward(q_host, o_host, kv_host):
                                   o_on_host=o_host)
     up.upipe_sync_status()
     assert (not o2.is_cuda) == o_host
+    ro, rl = oracle.attn_fwd_ref(q, k, v, causal=True)
+    err_o, err_l = max_abs(to_np(o2), ro), max_abs(to_np(l2), rl)
+    assert err_o <= O_MAX_ABS and err_l <= LSE_MAX_ABS, (err_o, err_l)
     assert torch.equal(o1.cpu(), o2.cpu()) and torch.equal(l1, l2)
 
 
