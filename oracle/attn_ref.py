@@ -40,6 +40,8 @@ __all__ = [
     "attn_rows_ref",
     "attn_dkdv_window_ref",
     "attn_group_ref",
+    "attn_row_stats_ref",
+    "attn_group_from_stats_ref",
     "attn_fwd_trunked_ref",
     "attn_bwd_trunked_ref",
 ]
@@ -298,6 +300,121 @@ def attn_group_ref(q, k, v, dout, b, kvh, causal=True, scale=None, key_lo=0, key
                 dv[: w1 - key_lo] += P[:, key_lo:w1].T @ dOb
     rows = np.arange(row_lo, S) if want_rows else np.zeros(0, dtype=np.int64)
     return rows, o.numpy(), lse.numpy(), dq.numpy(), dk.numpy(), dv.numpy()
+
+
+def attn_row_stats_ref(q, k, v, dout, b, h, row_lo, row_hi, causal=True, scale=None,
+                       row_block=512):
+    """The two per-row statistics the backward pass needs, for query rows [row_lo, row_hi) of
+    (batch b, q-head h): LSE_i = max_j s_ij + ln sum_j exp(s_ij - max) and D_i = <dO_i, O_i>,
+    each row's softmax taken over its full key range (the definition, as in attn_bwd_ref),
+    with PyTorch's fp64 CPU operations. Returns (lse [n], dvec [n]) as fp64 numpy arrays.
+
+    This is the expensive half of a backward check at S >= 128K: the statistics of every row
+    that sees a key window need that row's full score row and O_i."""
+    import torch
+
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    kvh = h // (Hq // Hkv)
+    sc = _scale(D, scale)
+    f64 = torch.float64
+
+    def rows_of(x, hh, lo, hi):
+        t = torch.as_tensor(x) if not hasattr(x, "detach") else x.detach()
+        return t[b, lo:hi, hh, :].to("cpu").to(f64)
+
+    m_all = row_hi if causal else S
+    K = rows_of(k, kvh, 0, m_all)
+    V = rows_of(v, kvh, 0, m_all)
+    Q = rows_of(q, h, row_lo, row_hi)
+    dO = rows_of(dout, h, row_lo, row_hi)
+    lse = torch.empty(row_hi - row_lo, dtype=f64)
+    dvec = torch.empty(row_hi - row_lo, dtype=f64)
+    for i0 in range(row_lo, row_hi, row_block):
+        i1 = min(row_hi, i0 + row_block)
+        m = i1 if causal else S
+        r = slice(i0 - row_lo, i1 - row_lo)
+        s = torch.mm(Q[r], K[:m].T).mul_(sc)
+        if causal:
+            j = torch.arange(i0, m)[None, :]
+            i = torch.arange(i0, i1)[:, None]
+            s[:, i0:].masked_fill_(j > i, float("-inf"))
+        mx = s.max(dim=1, keepdim=True).values
+        P = s.sub_(mx).exp_()
+        l = P.sum(dim=1, keepdim=True)
+        P.div_(l)
+        lse[r] = (mx + torch.log(l))[:, 0]
+        dvec[r] = (dO[r] * (P @ V[:m])).sum(dim=1)
+    return lse.numpy(), dvec.numpy()
+
+
+def attn_group_from_stats_ref(q, k, v, dout, b, kvh, lse, dvec, row_lo, key_lo=0, key_hi=None,
+                              causal=True, scale=None, want_dq=False, row_block=512):
+    """The backward of one (batch b, kv-head kvh) slice from given row statistics.
+
+    lse, dvec: [G, S - row_lo] fp64, LSE_i and D_i of rows [row_lo, S) of the group's q-heads
+    (from attn_row_stats_ref). With P_ij = exp(s_ij - LSE_i) (the probabilities recomputed
+    from the saved statistic, as the FPDT talk's Background describes the attention backward)
+    and dS_ij = P_ij (dP_ij - D_i), returns
+      dK_j = scale sum_h sum_i dS_ij q_i and dV_j = sum_h sum_i P_ij dO_i for keys
+      [key_lo, key_hi), and, with want_dq, dQ_i = scale sum_j dS_ij k_j for rows [row_lo, S).
+    Causal rows below key_lo see no key of the window, so row_lo <= key_lo suffices (row_lo
+    must be 0 when not causal). Returns (dk [m, D], dv [m, D], dq [S - row_lo, G, D] or None)
+    as fp64 numpy arrays; PyTorch fp64 CPU operations."""
+    import torch
+
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    G = Hq // Hkv
+    sc = _scale(D, scale)
+    key_hi = S if key_hi is None else int(key_hi)
+    if row_lo > (key_lo if causal else 0):
+        raise ValueError("rows below row_lo would see the key window")
+    f64 = torch.float64
+
+    def rows_of(x, hh, lo, hi):
+        t = torch.as_tensor(x) if not hasattr(x, "detach") else x.detach()
+        return t[b, lo:hi, hh, :].to("cpu").to(f64)
+
+    lse = torch.as_tensor(np.asarray(lse, dtype=np.float64))
+    dvec = torch.as_tensor(np.asarray(dvec, dtype=np.float64))
+    K = rows_of(k, kvh, 0, S)
+    V = rows_of(v, kvh, 0, S)
+    dk = torch.zeros((key_hi - key_lo, D), dtype=f64)
+    dv = torch.zeros((key_hi - key_lo, D), dtype=f64)
+    dq = torch.zeros((S - row_lo, G, D), dtype=f64) if want_dq else None
+    # rows that matter: all given rows for dQ; else those that see the window
+    first_row = row_lo if want_dq else (key_lo if causal else 0)
+    for g in range(G):
+        h = kvh * G + g
+        Q = rows_of(q, h, row_lo, S)
+        dO = rows_of(dout, h, row_lo, S)
+        for i0 in range(first_row, S, row_block):
+            i1 = min(S, i0 + row_block)
+            r = slice(i0 - row_lo, i1 - row_lo)
+            # key columns this block needs: every visible key (for dQ) or the window's
+            visible = i1 if causal else S
+            c0 = 0 if want_dq else key_lo
+            c1 = visible if want_dq else min(key_hi, visible)
+            if c1 <= c0:
+                continue
+            s = torch.mm(Q[r], K[c0:c1].T).mul_(sc)
+            s.sub_(lse[g, r][:, None])
+            if causal:  # columns j >= i0 can lie above a row of this block
+                lo = max(c0, i0)
+                if lo < c1:
+                    j = torch.arange(lo, c1)[None, :]
+                    i = torch.arange(i0, i1)[:, None]
+                    s[:, lo - c0:].masked_fill_(j > i, float("-inf"))
+            P = s.exp_()
+            dS = torch.mm(dO[r], V[c0:c1].T).sub_(dvec[g, r][:, None]).mul_(P)
+            if want_dq:
+                dq[r, g] = sc * (dS @ K[c0:c1])
+            w0, w1 = max(key_lo, c0), min(key_hi, c1)
+            if w1 > w0:
+                dk[w0 - key_lo:w1 - key_lo] += sc * (dS[:, w0 - c0:w1 - c0].T @ Q[r])
+                dv[w0 - key_lo:w1 - key_lo] += P[:, w0 - c0:w1 - c0].T @ dO[r]
+    return dk.numpy(), dv.numpy(), (dq.numpy() if want_dq else None)
 
 
 # ----------------------------------------------------------------------------------------

@@ -312,6 +312,40 @@ def test_group_slice_matches_full(causal, key_lo, key_hi, want_rows):
         np.testing.assert_allclose(gdq, dq[b, rows, hs], rtol=0, atol=1e-13)
 
 
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("row_lo,key_lo,key_hi,want_dq", [(0, 0, None, True), (0, 23, 41, False),
+                                                          (17, 23, 41, False), (23, 60, 70, True),
+                                                          (0, 0, 70, False)])
+def test_backward_from_row_statistics_matches_full(causal, row_lo, key_lo, key_hi, want_dq):
+    """Splitting the backward into per-row statistics (LSE_i, D_i: the expensive forward half)
+    and the dK/dV/dQ pass from them gives the slices of the pinned numpy oracle."""
+    if not causal:
+        row_lo = 0
+    q, k, v, do = random_small(2, 70, 6, 2, 8, 29)
+    o, lse, dq, dk, dv = ref.attn_bwd_ref(q, k, v, do, causal=causal)
+    G = 3
+    for b, kvh in ((0, 1), (1, 0)):
+        hs = list(range(kvh * G, (kvh + 1) * G))
+        st = [ref.attn_row_stats_ref(q, k, v, do, b, h, row_lo, 70, causal=causal, row_block=11)
+              for h in hs]
+        sl = np.stack([x[0] for x in st])
+        sd = np.stack([x[1] for x in st])
+        np.testing.assert_allclose(sl, lse[b][hs, row_lo:], rtol=0, atol=1e-13)
+        want_d = np.einsum("ihd,ihd->hi", _np(do)[b][row_lo:, hs], o[b][row_lo:, hs])
+        np.testing.assert_allclose(sd, want_d, rtol=0, atol=1e-12)
+        gdk, gdv, gdq = ref.attn_group_from_stats_ref(q, k, v, do, b, kvh, sl, sd, row_lo,
+                                                      key_lo=key_lo, key_hi=key_hi,
+                                                      causal=causal, want_dq=want_dq,
+                                                      row_block=9)
+        hi = 70 if key_hi is None else key_hi
+        np.testing.assert_allclose(gdk, dk[b, key_lo:hi, kvh], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(gdv, dv[b, key_lo:hi, kvh], rtol=0, atol=1e-12)
+        if want_dq:
+            np.testing.assert_allclose(gdq, dq[b][row_lo:, hs], rtol=0, atol=1e-12)
+        else:
+            assert gdq is None
+
+
 def test_group_slice_closed_form_and_sdpa():
     """Two pins independent of the numpy oracle: with Q = 0 every causal row is the prefix
     mean of V, LSE_i = ln(i+1), dK = 0 and dV_j = sum_{i>=j} dO_i/(i+1) summed over the
