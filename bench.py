@@ -565,6 +565,7 @@ def run_sweep(a):
         grid = [(hc, T) for hc in ints(a.head_chunks, [a.head_chunk or w.head_chunk])
                 for T in ints(a.seq_trunks, [a.seq_trunk or w.seq_trunk])]
         kv_modes = (a.kv_modes or "device,host").split(",")
+    device_ms = {}
     for mode in kv_modes:
         kv_host = mode in ("host", "host+dkdv", "all")
         dkdv_host = mode in ("host+dkdv", "all")
@@ -628,6 +629,37 @@ def run_sweep(a):
                 tf += e[0].elapsed_time(e[1])
                 tb += e[1].elapsed_time(e[2])
             up.upipe_sync_status()
+            ms_step = (tf + tb) / a.steps
+            if mode == "device":
+                device_ms[(hc, T)] = ms_step
+            copies = {}
+            if kv_host:
+                # one more step with the library's event bracketing on: the copy stream's busy
+                # time per staged key/value trunk (and dK/dV trunk) against the kernels' time
+                up.upipe_profile_read()
+                up.upipe_profile_enable(True)
+                e[0].record()
+                fwd()
+                bwd()
+                e[1].record()
+                torch.cuda.synchronize()
+                up.upipe_profile_enable(False)
+                st = up.upipe_profile_read()
+                kv_ms, kv_n = st["kv_h2d"]
+                kv_bytes = 2 * (k.numel() + v.numel()) * k.element_size()  # fwd and bwd pass
+                kern_ms = sum(st[c][0] for c in ("layout", "attn_fwd", "bwd_pre", "attn_bwd",
+                                                 "dq_convert"))
+                copies = {
+                    "profiled_step_ms": e[0].elapsed_time(e[1]),
+                    "kernel_ms": kern_ms,
+                    "kv_h2d_ms": kv_ms, "kv_h2d_trunks": kv_n,
+                    "kv_h2d_gbs": kv_bytes / (kv_ms * 1e-3) / 1e9 if kv_ms else None,
+                    "dkdv_d2h_ms": st["dkdv_d2h"][0], "dkdv_d2h_trunks": st["dkdv_d2h"][1],
+                }
+                if (hc, T) in device_ms:
+                    # what staging adds to the step over the device-resident run: the copy
+                    # time the compute stream could not hide
+                    copies["exposed_copy_ms"] = ms_step - device_ms[(hc, T)]
             ff, fb = w.flops_fwd() * a.steps, w.flops_bwd() * a.steps
             print(json.dumps({
                 "sweep": a.sweep, "workload": w.name, "S": w.S, "head_chunk": hc,
@@ -635,7 +667,7 @@ def run_sweep(a):
                 "activations_on_host": act_host,
                 "fwd_tflops": ff / tf / 1e9,
                 "bwd_tflops": fb / tb / 1e9, "fwdbwd_tflops": (ff + fb) / (tf + tb) / 1e9,
-                "ms_per_step": (tf + tb) / a.steps, "workspace_gb": ws_b / 1e9,
+                "ms_per_step": ms_step, **copies, "workspace_gb": ws_b / 1e9,
                 "workspace_unchunked_gb": up.upipe_workspace_bytes(
                     w.B, w.S, w.Hq, w.Hkv, w.D, 1, w.Hq, T, up.UPIPE_PASS_BOTH, mask) / 1e9,
                 "device_bytes_allocated_by_calls": int(lib_alloc)}), flush=True)

@@ -141,6 +141,15 @@ void launch_begin(int kclass, cudaStream_t stream) {
   if (g_pending_e0) cudaEventRecord(g_pending_e0, stream);
 }
 
+void copy_begin(cudaStream_t stream) {
+  if (!g_profile.load(std::memory_order_relaxed)) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_pending_e0 = pool_event();
+  if (g_pending_e0) cudaEventRecord(g_pending_e0, stream);
+}
+
+void copy_end(int kclass, cudaStream_t stream) { launch_end(kclass, stream); }
+
 void launch_end(int kclass, cudaStream_t stream) {
   if (!g_profile.load(std::memory_order_relaxed) || !g_pending_e0) return;
   std::lock_guard<std::mutex> lk(g_prof_mu);
@@ -149,6 +158,22 @@ void launch_end(int kclass, cudaStream_t stream) {
   cudaEventRecord(e1, stream);
   g_prof.push_back({kclass, g_pending_e0, e1});
   g_pending_e0 = nullptr;
+}
+
+// ---- per-device kernel attributes --------------------------------------------------------
+cudaError_t ensure_smem_attr(const void* kernel, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static std::mutex mu;
+  static std::vector<std::pair<const void*, int>> done;  // (kernel, device) already set
+  std::lock_guard<std::mutex> lk(mu);
+  for (const auto& d : done)
+    if (d.first == kernel && d.second == dev) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  done.emplace_back(kernel, dev);
+  return cudaSuccess;
 }
 
 // ---- tensor maps ----------------------------------------------------------------------------
@@ -187,27 +212,13 @@ namespace {
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
-struct Plan {
-  int B = 0, Hq = 0, Hkv = 0, D = 0, G = 0, hc = 0, kc = 0, causal = 1;
-  int64_t S = 0, T = 0, S_pad = 0, T_pad = 0;
-  int n_trunks = 0;
-  bool kv_host = false;
-  bool act_host = false;  // q/o (and dout/dq) may be pinned host memory: staging reserved
-  // forward segments
-  size_t f_qw = 0, f_kw = 0, f_vw = 0, f_slot_k[2] = {0, 0}, f_slot_v[2] = {0, 0};
-  size_t f_qw2 = 0, f_ostg[2] = {0, 0};  // host activations: second Q buffer, O staging
-  size_t f_state_o = 0, f_state_ml = 0, f_total = 0;
-  // backward segments
-  size_t b_qw = 0, b_dow = 0, b_kw = 0, b_vw = 0, b_slot_k[2] = {0, 0}, b_slot_v[2] = {0, 0};
-  size_t b_slot_dk[2] = {0, 0}, b_slot_dv[2] = {0, 0};  // host-K/V mode: dK/dV trunk slots
-  // host activations: second Q and dO buffers, head-major O copies, dQ output stagings
-  size_t b_qw2 = 0, b_dow2 = 0, b_ow[2] = {0, 0}, b_dqs[2] = {0, 0};
-  size_t b_dqacc = 0, b_lse2 = 0, b_dvec = 0, b_total = 0;
-};
+using Plan = AttnPlan;
+
+}  // namespace
 
 // Validates shapes (no device access). Returns UPIPE_OK and fills the plan.
-int make_plan(int B, int64_t S, int Hq, int Hkv, int D, int causal, int head_chunk,
-              int64_t seq_trunk, int host_mask, Plan* p) {
+int make_attn_plan(int B, int64_t S, int Hq, int Hkv, int D, int causal, int head_chunk,
+                   int64_t seq_trunk, int host_mask, AttnPlan* p) {
   if (B < 1 || S < 1 || Hq < 1 || Hkv < 1 || D < 1)
     return fail(UPIPE_ERR_INVALID_ARG, "sizes must be positive (B=%d S=%lld Hq=%d Hkv=%d D=%d)",
                 B, static_cast<long long>(S), Hq, Hkv, D);
@@ -257,13 +268,12 @@ int make_plan(int B, int64_t S, int Hq, int Hkv, int D, int causal, int head_chu
     p->f_kw = take(kvw);
     p->f_vw = take(kvw);
   }
-  if (p->n_trunks > 1) {
+  if (p->kv_host && p->n_trunks > 1) {
     // Host K/V: the forward walks key/value trunks outermost (each trunk is staged once), so
-    // the running state of every query trunk is kept: S_pad rows. Device K/V: one query
-    // trunk at a time, T_pad rows.
-    const int64_t rows = p->kv_host ? p->S_pad : p->T_pad;
-    p->f_state_o = take(hcB * rows * D * 4);
-    p->f_state_ml = take(hcB * rows * 2 * 4);
+    // the running state of every query trunk is kept between launches: S_pad rows. Device
+    // K/V need none: one launch walks every trunk with the state on chip.
+    p->f_state_o = take(hcB * p->S_pad * D * 4);
+    p->f_state_ml = take(hcB * p->S_pad * 2 * 4);
   }
   p->f_total = off;
   // backward
@@ -290,6 +300,8 @@ int make_plan(int B, int64_t S, int Hq, int Hkv, int D, int causal, int head_chu
   p->b_total = off;
   return UPIPE_OK;
 }
+
+namespace {
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
@@ -396,6 +408,22 @@ int unstage_heads(const void* stg, void* dst, int B, int64_t S, int H, int D, in
   return UPIPE_OK;
 }
 
+// Up to three head-group gathers, issued as one launch.
+struct GatherList {
+  const void* src[3];
+  void* dst[3];
+  int H[3], h0[3], count[3];
+  int n = 0;
+  void add(const void* s, void* d, int heads, int first, int cnt) {
+    src[n] = s; dst[n] = d; H[n] = heads; h0[n] = first; count[n] = cnt;
+    ++n;
+  }
+  cudaError_t launch(int B, int64_t S, int D, cudaStream_t stream) const {
+    if (n == 0) return cudaSuccess;
+    return launch_gather_group(src, dst, H, h0, count, n, B, S, D, stream);
+  }
+};
+
 // Double-buffered trunk stager shared by forward and backward.
 struct Stager {
   const Plan& p;
@@ -415,9 +443,10 @@ struct Stager {
     const int64_t t0 = static_cast<int64_t>(j.n) * p.T;
     const int64_t Tn = std::min<int64_t>(p.T, p.S - t0);
     UPIPE_CUDA(cudaStreamWaitEvent(ds->copy, ds->slot_free[s], 0));
+    copy_begin(ds->copy);
     int st = stage_trunk(p, k, slot_k[s], j.kvh0, t0, Tn, ds->copy);
-    if (st != UPIPE_OK) return st;
-    st = stage_trunk(p, v, slot_v[s], j.kvh0, t0, Tn, ds->copy);
+    if (st == UPIPE_OK) st = stage_trunk(p, v, slot_v[s], j.kvh0, t0, Tn, ds->copy);
+    copy_end(UPIPE_K_KV_H2D, ds->copy);
     if (st != UPIPE_OK) return st;
     UPIPE_CUDA(cudaEventRecord(ds->slot_ready[s], ds->copy));
     return UPIPE_OK;
@@ -468,6 +497,28 @@ int device_status_word(int dev, uint32_t** err) {
   return UPIPE_OK;
 }
 
+cudaError_t launch_fwd_resident(const AttnPlan& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                                const CUtensorMap& tv, int h0, void* o, int o_heads, float* lse,
+                                uint32_t* err, cudaStream_t stream) {
+  FwdArgs a{};
+  a.q_lo = 0;
+  a.q_hi = p.S;
+  a.kv_row_lo = 0;
+  a.kv_row_hi = p.S;
+  a.kv_pos0 = 0;
+  a.S = p.S;
+  a.hc = p.hc; a.kc = p.kc; a.G = p.G; a.Hq = p.Hq; a.h0 = h0;
+  a.causal = p.causal; a.first = 1; a.last = 1;
+  const float scale = 1.0f / std::sqrt(static_cast<float>(p.D));
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.o = o; a.lse = lse;
+  a.o_heads = o_heads; a.o_head0 = 0;
+  a.state_o = nullptr; a.state_ml = nullptr;
+  a.state_rows = 0; a.state_stride = 0;
+  a.err = err;
+  return launch_attn_fwd(p.D, p.B, tq, tk, tv, a, stream);
+}
+
 }  // namespace upipe
 
 using namespace upipe;
@@ -477,7 +528,7 @@ extern "C" {
 size_t upipe_workspace_bytes(int B, int64_t S, int Hq, int Hkv, int D, int causal,
                              int head_chunk, int64_t seq_trunk, int pass, int host_mask) {
   Plan p;
-  if (make_plan(B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk, host_mask, &p) != UPIPE_OK)
+  if (make_attn_plan(B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk, host_mask, &p) != UPIPE_OK)
     return 0;
   if (pass == UPIPE_PASS_FWD) return p.f_total;
   if (pass == UPIPE_PASS_BWD) return p.b_total;
@@ -498,7 +549,7 @@ int upipe_attn_fwd(const void* q, const void* k, const void* v, void* o, float* 
   if (reinterpret_cast<uintptr_t>(workspace) % kAlign)
     return fail(UPIPE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   Plan p0;
-  int st = make_plan(B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk, 0, &p0);
+  int st = make_attn_plan(B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk, 0, &p0);
   if (st != UPIPE_OK) return st;
   // q and o: device memory of the call's device, or pinned host memory (each on its own)
   int dq_dev = -1, do_dev = -1;
@@ -521,21 +572,23 @@ int upipe_attn_fwd(const void* q, const void* k, const void* v, void* o, float* 
   st = check_placement(dlist, nd, nlist, k, v, &kv_host, &dev);
   if (st != UPIPE_OK) return st;
   Plan p;
-  make_plan(B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk,
+  make_attn_plan(B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk,
             (kv_host ? UPIPE_HOST_KV : 0) | (q_host || o_host ? UPIPE_HOST_ACT : 0), &p);
   if (workspace_bytes < p.f_total)
     return fail(UPIPE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes,
                 p.f_total);
 
   std::lock_guard<std::mutex> lk(g_mu);
+  const DeviceGuard dguard;
   UPIPE_CUDA(cudaSetDevice(dev));
   DevState* ds = nullptr;
   st = dev_state(dev, &ds);
   if (st != UPIPE_OK) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  float* state_o = p.n_trunks > 1 ? reinterpret_cast<float*>(ws + p.f_state_o) : nullptr;
-  float* state_ml = p.n_trunks > 1 ? reinterpret_cast<float*>(ws + p.f_state_ml) : nullptr;
+  const bool carried = kv_host && p.n_trunks > 1;  // running state kept between launches
+  float* state_o = carried ? reinterpret_cast<float*>(ws + p.f_state_o) : nullptr;
+  float* state_ml = carried ? reinterpret_cast<float*>(ws + p.f_state_ml) : nullptr;
   const float scale = 1.0f / std::sqrt(static_cast<float>(D));
 
   Stager stg{p, ds, stream, k, v, {ws + p.f_slot_k[0], ws + p.f_slot_k[1]},
@@ -568,6 +621,7 @@ int upipe_attn_fwd(const void* q, const void* k, const void* v, void* o, float* 
   }
   // host o: group g's kernels write a [B, S, hc, D] staging buffer, copied out afterwards
   void* o_out = o;
+  // Host K/V: one launch per (key/value trunk n, query trunk m), the state in the arena.
   auto launch = [&](const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, int h0,
                     int m, int n, int64_t row_lo, int64_t row_hi, int64_t pos0,
                     int64_t state_stride) -> int {
@@ -605,32 +659,32 @@ int upipe_attn_fwd(const void* q, const void* k, const void* v, void* o, float* 
         if (st != UPIPE_OK) return st;
       }
       UPIPE_CUDA(cudaStreamWaitEvent(stream, ds->act_ready[gs], 0));
-    } else {
-      UPIPE_CUDA(launch_seq_to_head(q, qwg, B, S, Hq, D, h0, p.hc, stream));
     }
     if (o_host) {
       // the staging this group writes must have reached the host from group g-2
       if (g >= 2) UPIPE_CUDA(cudaStreamWaitEvent(stream, ds->out_free[gs], 0));
       o_out = ws + p.f_ostg[gs];
     }
-    if (!kv_host) {
-      UPIPE_CUDA(launch_seq_to_head(k, ws + p.f_kw, B, S, Hkv, D, kvh0, p.kc, stream));
-      UPIPE_CUDA(launch_seq_to_head(v, ws + p.f_vw, B, S, Hkv, D, kvh0, p.kc, stream));
+    {
+      // the group's device-resident Q, K and V gathered head-major in one launch
+      GatherList gl;
+      if (!q_host) gl.add(q, qwg, Hq, h0, p.hc);
+      if (!kv_host) {
+        gl.add(k, ws + p.f_kw, Hkv, kvh0, p.kc);
+        gl.add(v, ws + p.f_vw, Hkv, kvh0, p.kc);
+      }
+      UPIPE_CUDA(gl.launch(B, S, D, stream));
     }
     CUtensorMap tq, tk, tv;
     UPIPE_CUDA(make_tmap_bf16(&tq, qwg, D, S, static_cast<int64_t>(B) * p.hc));
     if (!kv_host) {
-      // FPDT order: query trunk m folds key/value trunks 0..m into a T-row state
+      // Device-resident K/V: one launch folds every key/value trunk into every query row, the
+      // running softmax state of each query tile staying in TMEM and registers from the first
+      // key tile to the last (FPDT's trunk loop, run inside the kernel).
       UPIPE_CUDA(make_tmap_bf16(&tk, ws + p.f_kw, D, S, static_cast<int64_t>(B) * p.kc));
       UPIPE_CUDA(make_tmap_bf16(&tv, ws + p.f_vw, D, S, static_cast<int64_t>(B) * p.kc));
-      for (int m = 0; m < p.n_trunks; ++m) {
-        const int n_last = causal ? m : p.n_trunks - 1;
-        for (int n = 0; n <= n_last; ++n) {
-          const int64_t t0 = static_cast<int64_t>(n) * p.T;
-          st = launch(tq, tk, tv, h0, m, n, t0, std::min<int64_t>(S, t0 + p.T), 0, 0);
-          if (st != UPIPE_OK) return st;
-        }
-      }
+      UPIPE_CUDA(launch_fwd_resident(p, tq, tk, tv, h0, o_out, o_host ? p.hc : 0, lse, ds->err,
+                                     stream));
     } else {
       // Host K/V: key/value trunk n is staged once and then met by every query trunk that
       // sees it (m >= n when causal); each query trunk keeps its running state in an S-sized
@@ -683,7 +737,7 @@ int upipe_attn_bwd(const void* q, const void* k, const void* v, const void* o, c
   if (reinterpret_cast<uintptr_t>(workspace) % kAlign)
     return fail(UPIPE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   Plan p0;
-  int st = make_plan(B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk, 0, &p0);
+  int st = make_attn_plan(B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk, 0, &p0);
   if (st != UPIPE_OK) return st;
   // q, o, dout, dq: device memory of the call's device, or pinned host memory (each on its own)
   const void* act[4] = {q, o, dout, dq};
@@ -724,13 +778,14 @@ int upipe_attn_bwd(const void* q, const void* k, const void* v, const void* o, c
   if (dkdv_host && !kv_host)
     return fail(UPIPE_ERR_INVALID_ARG, "dk/dv may be pinned host memory only when k/v are too");
   Plan p;
-  make_plan(B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk,
+  make_attn_plan(B, S, Hq, Hkv, D, causal, head_chunk, seq_trunk,
             (kv_host ? UPIPE_HOST_KV : 0) | (any_act ? UPIPE_HOST_ACT : 0), &p);
   if (workspace_bytes < p.b_total)
     return fail(UPIPE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes,
                 p.b_total);
 
   std::lock_guard<std::mutex> lk(g_mu);
+  const DeviceGuard dguard;
   UPIPE_CUDA(cudaSetDevice(dev));
   DevState* ds = nullptr;
   st = dev_state(dev, &ds);
@@ -794,7 +849,15 @@ int upipe_attn_bwd(const void* q, const void* k, const void* v, const void* o, c
       }
       UPIPE_CUDA(cudaStreamWaitEvent(stream, ds->act_ready[gs], 0));
     }
-    if (!q_host) UPIPE_CUDA(launch_seq_to_head(q, qw, B, S, Hq, D, h0, p.hc, stream));
+    {
+      GatherList gl;
+      if (!q_host) gl.add(q, qw, Hq, h0, p.hc);
+      if (!kv_host) {
+        gl.add(k, ws + p.b_kw, Hkv, kvh0, p.kc);
+        gl.add(v, ws + p.b_vw, Hkv, kvh0, p.kc);
+      }
+      UPIPE_CUDA(gl.launch(B, S, D, stream));
+    }
     if (hm_pre) {
       void* ow = ow_of(g);
       if (!o_host) UPIPE_CUDA(launch_seq_to_head(o, ow, B, S, Hq, D, h0, p.hc, stream));
@@ -805,10 +868,6 @@ int upipe_attn_bwd(const void* q, const void* k, const void* v, const void* o, c
       UPIPE_CUDA(launch_bwd_pre(o, dout, lse, dow, dvec, lse2, dqacc, B, S, p.S_pad, Hq, D, h0,
                                 p.hc, scale, 0, stream));
     }
-    if (!kv_host) {
-      UPIPE_CUDA(launch_seq_to_head(k, ws + p.b_kw, B, S, Hkv, D, kvh0, p.kc, stream));
-      UPIPE_CUDA(launch_seq_to_head(v, ws + p.b_vw, B, S, Hkv, D, kvh0, p.kc, stream));
-    }
     CUtensorMap tq, tdo, tk, tv;
     UPIPE_CUDA(make_tmap_bf16(&tq, qw, D, S, static_cast<int64_t>(B) * p.hc, bwd_q_box_rows(D)));
     UPIPE_CUDA(make_tmap_bf16(&tdo, dow, D, S, static_cast<int64_t>(B) * p.hc, bwd_q_box_rows(D)));
@@ -816,9 +875,14 @@ int upipe_attn_bwd(const void* q, const void* k, const void* v, const void* o, c
       UPIPE_CUDA(make_tmap_bf16(&tk, ws + p.b_kw, D, S, static_cast<int64_t>(B) * p.kc));
       UPIPE_CUDA(make_tmap_bf16(&tv, ws + p.b_vw, D, S, static_cast<int64_t>(B) * p.kc));
     }
-    for (int n = 0; n < p.n_trunks; ++n, ++job) {
-      const int64_t t0 = static_cast<int64_t>(n) * p.T;
-      const int64_t Tn = std::min<int64_t>(p.T, S - t0);
+    // Host K/V: one launch per key/value trunk (each staged once). Device-resident K/V: one
+    // launch over every key tile; each CTA's walk over the query tiles that see its key tile
+    // is the same either way, so only the number of launches differs.
+    const int n_launch = kv_host ? p.n_trunks : 1;
+    const int64_t T_launch = kv_host ? p.T : S;
+    for (int n = 0; n < n_launch; ++n, ++job) {
+      const int64_t t0 = static_cast<int64_t>(n) * T_launch;
+      const int64_t Tn = std::min<int64_t>(T_launch, S - t0);
       BwdArgs a{};
       a.S = S; a.S_pad = p.S_pad;
       a.hc = p.hc; a.kc = p.kc; a.G = p.G; a.Hkv = Hkv; a.kvh0 = kvh0;
@@ -852,9 +916,10 @@ int upipe_attn_bwd(const void* q, const void* k, const void* v, const void* o, c
         // this trunk's dK/dV are final: copy them out on the copy stream
         UPIPE_CUDA(cudaEventRecord(ds->dkdv_done[s], stream));
         UPIPE_CUDA(cudaStreamWaitEvent(ds->copy, ds->dkdv_done[s], 0));
+        copy_begin(ds->copy);
         st = unstage_trunk(p, ws + p.b_slot_dk[s], dk, kvh0, t0, Tn, ds->copy);
-        if (st != UPIPE_OK) return st;
-        st = unstage_trunk(p, ws + p.b_slot_dv[s], dv, kvh0, t0, Tn, ds->copy);
+        if (st == UPIPE_OK) st = unstage_trunk(p, ws + p.b_slot_dv[s], dv, kvh0, t0, Tn, ds->copy);
+        copy_end(UPIPE_K_DKDV_D2H, ds->copy);
         if (st != UPIPE_OK) return st;
         UPIPE_CUDA(cudaEventRecord(ds->dkdv_free[s], ds->copy));
       }
@@ -887,7 +952,7 @@ int upipe_attn_bwd(const void* q, const void* k, const void* v, const void* o, c
 }
 
 static int layout_args(const void* src, const void* dst, int B, int64_t S, int H, int D,
-                       int h_begin, int h_count) {
+                       int h_begin, int h_count, int* dev) {
   if (!src || !dst) return fail(UPIPE_ERR_INVALID_ARG, "null pointer argument");
   if (!aligned16(src) || !aligned16(dst))
     return fail(UPIPE_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
@@ -900,15 +965,18 @@ static int layout_args(const void* src, const void* dst, int B, int64_t S, int H
   int d1 = -1, d2 = -1;
   if (pointer_kind(src, &d1) != 0 || pointer_kind(dst, &d2) != 0 || d1 != d2)
     return fail(UPIPE_ERR_INVALID_ARG, "src and dst must be memory of one device");
-  UPIPE_CUDA(cudaSetDevice(d1));
+  *dev = d1;
   return UPIPE_OK;
 }
 
 int upipe_seq_to_head_major(const void* src, void* dst, int B, int64_t S, int H, int D,
                             int h_begin, int h_count, void* stream) {
   g_last_error.clear();
-  const int st = layout_args(src, dst, B, S, H, D, h_begin, h_count);
+  int dev = 0;
+  const int st = layout_args(src, dst, B, S, H, D, h_begin, h_count, &dev);
   if (st != UPIPE_OK) return st;
+  const DeviceGuard dguard;
+  UPIPE_CUDA(cudaSetDevice(dev));
   UPIPE_CUDA(launch_seq_to_head(src, dst, B, S, H, D, h_begin, h_count,
                                 static_cast<cudaStream_t>(stream)));
   return UPIPE_OK;
@@ -917,8 +985,11 @@ int upipe_seq_to_head_major(const void* src, void* dst, int B, int64_t S, int H,
 int upipe_head_to_seq_major(const void* src, void* dst, int B, int64_t S, int H, int D,
                             int h_begin, int h_count, void* stream) {
   g_last_error.clear();
-  const int st = layout_args(src, dst, B, S, H, D, h_begin, h_count);
+  int dev = 0;
+  const int st = layout_args(src, dst, B, S, H, D, h_begin, h_count, &dev);
   if (st != UPIPE_OK) return st;
+  const DeviceGuard dguard;
+  UPIPE_CUDA(cudaSetDevice(dev));
   UPIPE_CUDA(launch_head_to_seq(src, dst, B, S, H, D, h_begin, h_count,
                                 static_cast<cudaStream_t>(stream)));
   return UPIPE_OK;
@@ -955,6 +1026,7 @@ const char* upipe_status_string(int status) {
 const char* upipe_last_error_message(void) { return g_last_error.c_str(); }
 
 void upipe_shutdown(void) {
+  const DeviceGuard dguard;
   upipe::seqtile_shutdown();
   std::lock_guard<std::mutex> lk(g_mu);
   for (int i = 0; i < kMaxDev; ++i) {
@@ -1034,6 +1106,7 @@ int upipe_selftest_umma(const void* a, const void* b, float* c, int N, int K, in
       dev != d2 || dev != d3)
     return fail(UPIPE_ERR_INVALID_ARG, "a, b, c must be memory of one device");
   std::lock_guard<std::mutex> lk(g_mu);
+  const DeviceGuard dguard;
   UPIPE_CUDA(cudaSetDevice(dev));
   DevState* ds = nullptr;
   const int st = dev_state(dev, &ds);

@@ -344,12 +344,10 @@ cudaError_t launch_impl(int B, const CUtensorMap& q_map, const CUtensorMap& do_m
                         const CUtensorMap& k_map, const CUtensorMap& v_map, const BwdArgs& a,
                         cudaStream_t stream) {
   using L = BwdLayout<D>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+  {
+    const cudaError_t e =
+        ensure_smem_attr(reinterpret_cast<const void*>(&attn_bwd_kernel<D>), L::kBytes);
     if (e != cudaSuccess) return e;
-    attr_done = true;
   }
   const int64_t n_kt = (a.kv_row_hi - a.kv_row_lo + 127) / 128;
   dim3 grid(static_cast<unsigned>(n_kt), static_cast<unsigned>(a.kc), static_cast<unsigned>(B));

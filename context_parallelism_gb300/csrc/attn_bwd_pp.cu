@@ -30,7 +30,7 @@
 //
 // Threads (512): warps 0-3 compute group 0, warps 4-7 compute group 1, warps 8-11 dQ drain,
 // warp 12 TMEM + MMA issue, warp 13 TMA producer, warps 14-15 idle. Registers move from the
-// drain to the compute groups (152 / 152 / 80 / 128 per thread).
+// MMA/TMA warpgroup to the compute groups and the drain (152 / 152 / 152 / 56 per thread).
 // TMEM: dV [0,128), dK [128,256), S [256,384), dP/dQ [384,512).
 // Shared memory (231.6 KB, no alignment slack: the dynamic window must start 1 KiB-aligned,
 // which is checked): K, V, two Q and two dO stages, dS^T, two LSE/D vector stages, barriers.
@@ -165,11 +165,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     q0 = static_cast<int64_t>(qt_lo + c.qt) * 128;
   };
 
-  // Launched with 512 x 128 registers. The MMA/TMA warpgroup keeps 128, the dQ drain gives up
-  // 48 and each compute group takes 24 more: 128 * (128 + 80 + 2 * 152) = 65536, exactly the
-  // launch's pool. Each role's code sits inside the branch that sets its count, so the compiler
-  // allocates that code for it.
+  // Launched with 512 x 128 registers. The MMA/TMA warpgroup gives up 72, the dQ drain and each
+  // compute group take 24 more: 128 * (56 + 3 * 152) = 65536, exactly the launch's pool. Each
+  // role's code sits inside the branch that sets its count, so the compiler allocates that code
+  // for it.
   if (warp >= 12) {
+  setmaxnreg_dec<56>();
   if (warp == 13) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
@@ -221,26 +222,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t id_kk = idesc_bf16(128, 128, false, false);  // S^T, dP^T
       const uint32_t id_kmn = idesc_bf16(128, 128, false, true);  // dV (A in TMEM), dK
       const uint32_t id_mnmn = idesc_bf16(128, 128, true, true);  // dQ^T = K^T dS^T
-      // Descriptors built once; stages and steps are constant offsets (16-byte units).
-      const uint64_t dKk = kdesc0(smem_u32(smem + L::kK)), dVk = kdesc0(smem_u32(smem + L::kV));
-      const uint64_t dKmn = mndesc0(smem_u32(smem + L::kK));
-      const uint64_t dQk0 = kdesc0(smem_u32(smem + L::kQ));
-      const uint64_t dQmn0 = mndesc0(smem_u32(smem + L::kQ));
-      const uint64_t dDOk0 = kdesc0(smem_u32(smem + L::kDO));
-      const uint64_t dDOmn0 = mndesc0(smem_u32(smem + L::kDO));
-      const uint64_t dDSk = kdesc0(smem_u32(smem + L::kDS));
-      const uint64_t dDSmn = mndesc0(smem_u32(smem + L::kDS));
+      // Every descriptor is one base descriptor (K-major or MN-major, at the start of shared
+      // memory) plus a compile-time offset in 16-byte units. The base goes through an opaque
+      // move at each use, so the compiler cannot precompute the 40 per-step descriptors of a
+      // tile into registers: this warpgroup runs on 56 registers.
+      const uint64_t base_k = kdesc0(smem_u32(smem));
+      const uint64_t base_mn = mndesc0(smem_u32(smem));
       constexpr uint32_t kStageU = kTile >> 4;
+      constexpr uint32_t uK = L::kK >> 4, uV = L::kV >> 4, uQ = L::kQ >> 4, uDO = L::kDO >> 4,
+                         uDS = L::kDS >> 4;
       bool ok = wait(kv_full, 0);
 
       auto issue_s = [&](int i) -> bool {
         const int st = i & 1;
         if (!wait(qf + st, (i >> 1) & 1)) return false;
         tc_fence_after();
-        const uint64_t dQ = dQk0 + st * kStageU;
+        const uint64_t bk = opaque_u64(base_k);
+        const uint32_t uq = uQ + st * kStageU;
 #pragma unroll
         for (int k16 = 0; k16 < 8; ++k16)
-          umma_f16_ss(tS, dKk + kstep(k16), dQ + kstep(k16), id_kk, k16 > 0 ? 1u : 0u);
+          umma_f16_ss(tS, bk + (uK + kstep(k16)), bk + (uq + kstep(k16)), id_kk,
+                      k16 > 0 ? 1u : 0u);
         umma_commit(s_full);
         return true;
       };
@@ -249,12 +251,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait(p_ready, i & 1)) return false;
         if (!wait(df + st, (i >> 1) & 1)) return false;
         tc_fence_after();
-        const uint64_t dDO = dDOmn0 + st * kStageU;
+        const uint64_t bmn = opaque_u64(base_mn);
+        const uint32_t udo = uDO + st * kStageU;
         const uint32_t acc0 = i > 0 ? 1u : 0u;
 #pragma unroll
         for (int k16 = 0; k16 < 8; ++k16)  // group 0's P^T at S+0, group 1's at S+64
-          umma_f16_ts(tDV, tS + (k16 >> 2) * 64 + (k16 & 3) * 8, dDO + mnstep(k16), id_kmn,
-                      k16 > 0 ? 1u : acc0);
+          umma_f16_ts(tDV, tS + (k16 >> 2) * 64 + (k16 & 3) * 8, bmn + (udo + mnstep(k16)),
+                      id_kmn, k16 > 0 ? 1u : acc0);
         umma_commit(de + st);
         return true;
       };
@@ -263,10 +266,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (i >= 1 && !wait(dq_free, (i - 1) & 1)) return false;
         if (!wait(df + st, (i >> 1) & 1)) return false;
         tc_fence_after();
-        const uint64_t dDO = dDOk0 + st * kStageU;
+        const uint64_t bk = opaque_u64(base_k);
+        const uint32_t udo = uDO + st * kStageU;
 #pragma unroll
         for (int k16 = 0; k16 < 8; ++k16)
-          umma_f16_ss(tDP, dVk + kstep(k16), dDO + kstep(k16), id_kk, k16 > 0 ? 1u : 0u);
+          umma_f16_ss(tDP, bk + (uV + kstep(k16)), bk + (udo + kstep(k16)), id_kk,
+                      k16 > 0 ? 1u : 0u);
         umma_commit(dp_full);
         return true;
       };
@@ -274,15 +279,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = i & 1;
         if (!wait(ds_ready, i & 1)) return false;
         tc_fence_after();
-        const uint64_t dQ = dQmn0 + st * kStageU;
+        const uint64_t bmn = opaque_u64(base_mn);
         const uint32_t acc0 = i > 0 ? 1u : 0u;
 #pragma unroll
         for (int k16 = 0; k16 < 8; ++k16)
-          umma_f16_ss(tDP, dKmn + mnstep(k16), dDSmn + mnstep(k16), id_mnmn, k16 > 0 ? 1u : 0u);
+          umma_f16_ss(tDP, bmn + (uK + mnstep(k16)), bmn + (uDS + mnstep(k16)), id_mnmn,
+                      k16 > 0 ? 1u : 0u);
         umma_commit(dq_full);
+        const uint64_t bk = opaque_u64(base_k);
+        const uint64_t bmn2 = opaque_u64(base_mn);
+        const uint32_t uq = uQ + st * kStageU;
 #pragma unroll
         for (int k16 = 0; k16 < 8; ++k16)
-          umma_f16_ss(tDK, dDSk + kstep(k16), dQ + mnstep(k16), id_kmn, k16 > 0 ? 1u : acc0);
+          umma_f16_ss(tDK, bk + (uDS + kstep(k16)), bmn2 + (uq + mnstep(k16)), id_kmn,
+                      k16 > 0 ? 1u : acc0);
         umma_commit(qe + st);
         return true;
       };
@@ -302,14 +312,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }  // warps 14-15: idle, they only complete the warpgroup of the MMA and TMA warps
   } else if (warp >= 8) {
-    setmaxnreg_dec<80>();
+    setmaxnreg_inc<152>();
     // ---------------- dQ drain ----------------
-    // dQ^T(i): lane t = head-dim index d, column c = query row q0 + c. Each warp adds one
-    // contiguous 128-byte line per query row, fire-and-forget: the first 64 columns, then the
-    // last 64, after which the columns are released (dP(i+1) reuses them; it is issued behind
-    // dV(i+1), which covers the first half's reductions). Query rows past S fall in the
-    // accumulator's padding (S_pad rows per head, a multiple of 128) and add exact zeros there
-    // (their P is masked to 0), so no bound check.
+    // dQ^T(i): lane t = head-dim index d, column c = query row q0 + c. The drain reads all 128
+    // columns into registers and releases them at once (dP(i+1) reuses them), then adds each
+    // query row's 128 floats as one contiguous 128-byte line per warp, fire-and-forget, while
+    // the tensor pipe already runs the next tile. Query rows past S fall in the accumulator's
+    // padding (S_pad rows per head, a multiple of 128) and add exact zeros there (their P is
+    // masked to 0), so no bound check.
     const int t = threadIdx.x & 127;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     Cursor cur;
@@ -320,16 +330,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       int64_t q0;
       decode(cur, zq, q0);
       float* dq_col = a.dqacc + (static_cast<int64_t>(zq) * a.S_pad + q0) * kD + t;
-      uint32_t r[64];
-      tmem_ld64_sync(tDP + lane_off, r);
-#pragma unroll
-      for (int x = 0; x < 64; ++x) red_add_f32(dq_col + x * kD, __uint_as_float(r[x]));
-      tmem_ld64_sync(tDP + lane_off + 64, r);
+      uint32_t ra[64], rb[64];
+      tmem_ld64_nowait(tDP + lane_off, ra);
+      tmem_ld64_nowait(tDP + lane_off + 64, rb);
+      tmem_wait_ld_dep64(ra);
+      tmem_reg_dep64(rb);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(dq_free);
 #pragma unroll
-      for (int x = 0; x < 64; ++x) red_add_f32(dq_col + (64 + x) * kD, __uint_as_float(r[x]));
+      for (int x = 0; x < 64; ++x) red_add_f32(dq_col + x * kD, __uint_as_float(ra[x]));
+#pragma unroll
+      for (int x = 0; x < 64; ++x) red_add_f32(dq_col + (64 + x) * kD, __uint_as_float(rb[x]));
     }
   } else {
     setmaxnreg_inc<152>();
@@ -487,13 +499,10 @@ cudaError_t launch_attn_bwd(int D, int B, const CUtensorMap& q_map, const CUtens
                             const CUtensorMap& k_map, const CUtensorMap& v_map,
                             const BwdArgs& a, cudaStream_t stream) {
   if (D != kD) return launch_attn_bwd_generic(D, B, q_map, do_map, k_map, v_map, a, stream);
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_pp_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         BppLayout::kBytes);
+  {
+    const cudaError_t e =
+        ensure_smem_attr(reinterpret_cast<const void*>(&attn_bwd_pp_kernel), BppLayout::kBytes);
     if (e != cudaSuccess) return e;
-    attr_done = true;
   }
   const int64_t n_kt = (a.kv_row_hi - a.kv_row_lo + 127) / 128;
   dim3 grid(static_cast<unsigned>(n_kt), static_cast<unsigned>(a.kc), static_cast<unsigned>(B));

@@ -374,12 +374,10 @@ template <int D>
 cudaError_t launch_impl(int B, const CUtensorMap& q_map, const CUtensorMap& k_map,
                         const CUtensorMap& v_map, const FwdArgs& a, cudaStream_t stream) {
   using L = FwdLayout<D>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+  {
+    const cudaError_t e =
+        ensure_smem_attr(reinterpret_cast<const void*>(&attn_fwd_kernel<D>), L::kBytes);
     if (e != cudaSuccess) return e;
-    attr_done = true;
   }
   const int64_t n_qt = (a.q_hi - a.q_lo + 127) / 128;
   dim3 grid(static_cast<unsigned>(n_qt), static_cast<unsigned>(a.hc), static_cast<unsigned>(B));

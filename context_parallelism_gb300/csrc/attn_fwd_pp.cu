@@ -396,13 +396,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t launch_attn_fwd(int D, int B, const CUtensorMap& q_map, const CUtensorMap& k_map,
                             const CUtensorMap& v_map, const FwdArgs& a, cudaStream_t stream) {
   if (D != kD) return launch_attn_fwd_generic(D, B, q_map, k_map, v_map, a, stream);
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_pp_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         FppLayout::kBytes);
+  {
+    const cudaError_t e =
+        ensure_smem_attr(reinterpret_cast<const void*>(&attn_fwd_pp_kernel), FppLayout::kBytes);
     if (e != cudaSuccess) return e;
-    attr_done = true;
   }
   const int64_t n_pairs = (a.q_hi - a.q_lo + 255) / 256;
   dim3 grid(static_cast<unsigned>(n_pairs), static_cast<unsigned>(a.hc), static_cast<unsigned>(B));

@@ -546,13 +546,10 @@ __global__ void ce_dlogits_kernel(const float* __restrict__ L, const float* __re
 template <int EPI, bool A_MN, bool B_MN>
 cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
                        int grid_cap, cudaStream_t stream) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI, A_MN, B_MN>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         GLayout::kBytes);
+  {
+    const cudaError_t e = ensure_smem_attr(
+        reinterpret_cast<const void*>(&gemm_tc_kernel<EPI, A_MN, B_MN>), GLayout::kBytes);
     if (e != cudaSuccess) return e;
-    configured = true;
   }
   constexpr int kOut = out_cols<EPI>();
   const int64_t tiles = static_cast<int64_t>((a.M + kBM - 1) / kBM) * ((a.N + kOut - 1) / kOut);

@@ -27,11 +27,69 @@ class NvtxRange {
   NvtxRange& operator=(const NvtxRange&) = delete;
 };
 
+// ---- attention workspace plan (api.cpp) ----------------------------------------------------
+// Byte offsets of every arena segment of the attention calls, each 256-byte aligned. f_* are
+// the forward's segments, b_* the backward's; *_total is each pass's size.
+struct AttnPlan {
+  int B = 0, Hq = 0, Hkv = 0, D = 0, G = 0, hc = 0, kc = 0, causal = 1;
+  int64_t S = 0, T = 0, S_pad = 0, T_pad = 0;
+  int n_trunks = 0;
+  bool kv_host = false;
+  bool act_host = false;  // q/o (and dout/dq) may be pinned host memory: staging reserved
+  // forward segments
+  size_t f_qw = 0, f_kw = 0, f_vw = 0, f_slot_k[2] = {0, 0}, f_slot_v[2] = {0, 0};
+  size_t f_qw2 = 0, f_ostg[2] = {0, 0};  // host activations: second Q buffer, O staging
+  size_t f_state_o = 0, f_state_ml = 0, f_total = 0;
+  // backward segments
+  size_t b_qw = 0, b_dow = 0, b_kw = 0, b_vw = 0, b_slot_k[2] = {0, 0}, b_slot_v[2] = {0, 0};
+  size_t b_slot_dk[2] = {0, 0}, b_slot_dv[2] = {0, 0};  // host-K/V mode: dK/dV trunk slots
+  // host activations: second Q and dO buffers, head-major O copies, dQ output stagings
+  size_t b_qw2 = 0, b_dow2 = 0, b_ow[2] = {0, 0}, b_dqs[2] = {0, 0};
+  size_t b_dqacc = 0, b_lse2 = 0, b_dvec = 0, b_total = 0;
+};
+
+
+// Validates the shape arguments of the attention calls (no device access) and fills the plan.
+// host_mask: UPIPE_HOST_KV / UPIPE_HOST_ACT reserve the staging segments of pinned-host tensors.
+// Returns UPIPE_OK, or UPIPE_ERR_INVALID_ARG / UPIPE_ERR_UNSUPPORTED with the reason recorded
+// for upipe_last_error_message().
+int make_attn_plan(int B, int64_t S, int Hq, int Hkv, int D, int causal, int head_chunk,
+                   int64_t seq_trunk, int host_mask, AttnPlan* p);
+
+// Raises a kernel's dynamic shared-memory limit to `bytes` on the current device, once per
+// (kernel, device): the attribute is per device, so a process that drives several GPUs sets it
+// on each. Thread-safe.
+cudaError_t ensure_smem_attr(const void* kernel, int bytes);
+
+// Restores the caller's current device when the scope ends (the entry points select the
+// device their tensors live on, and must not leave it changed).
+class DeviceGuard {
+ public:
+  DeviceGuard() {
+    if (cudaGetDevice(&prev_) != cudaSuccess) {
+      cudaGetLastError();
+      prev_ = -1;
+    }
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev_ >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev_) cudaSetDevice(prev_);
+  }
+  DeviceGuard(const DeviceGuard&) = delete;
+  DeviceGuard& operator=(const DeviceGuard&) = delete;
+
+ private:
+  int prev_ = -1;
+};
+
 // ---- launch bookkeeping (api.cpp) ---------------------------------------------------------
 // Every kernel launch goes through begin/end so the library can count launches and, when
 // profiling is on, bracket each one with CUDA events on its own stream.
 void launch_begin(int kclass, cudaStream_t stream);
 void launch_end(int kclass, cudaStream_t stream);
+// The same bracketing for a host<->device copy (profiling only; not a launch).
+void copy_begin(cudaStream_t stream);
+void copy_end(int kclass, cudaStream_t stream);
 
 // Records the message upipe_last_error_message() returns on this thread.
 void set_last_error(const char* msg);
@@ -67,6 +125,14 @@ cudaError_t launch_attn_fwd_generic(int D, int B, const CUtensorMap& q_map,
                                     const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_attn_fwd(int D, int B, const CUtensorMap& q_map, const CUtensorMap& k_map,
                             const CUtensorMap& v_map, const FwdArgs& a, cudaStream_t stream);
+
+// One forward launch over the whole sequence of head group h0..h0+hc-1 with device-resident,
+// head-major Q/K/V maps: every key/value trunk folded in with the running state on chip, O and
+// LSE finalised. o: token-major [B,S,Hq,D] (o_heads = 0) or a group staging [B,S,o_heads,D];
+// lse may be NULL (prefill). Used by upipe_attn_fwd and the no-allocation forward.
+cudaError_t launch_fwd_resident(const AttnPlan& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                                const CUtensorMap& tv, int h0, void* o, int o_heads, float* lse,
+                                uint32_t* err, cudaStream_t stream);
 
 // ---- backward attention (attn_bwd.cu) ------------------------------------------------------
 struct BwdArgs {
@@ -104,6 +170,11 @@ cudaError_t launch_attn_bwd(int D, int B, const CUtensorMap& q_map, const CUtens
 // dst[b][h][s][:] = src[b][s][h_begin + h][:]  for h < h_count   (bf16, D % 8 == 0)
 cudaError_t launch_seq_to_head(const void* src, void* dst, int B, int64_t S, int H, int D,
                                int h_begin, int h_count, cudaStream_t stream);
+// Up to three gathers in one launch: job i copies heads [h0[i], h0[i] + count[i]) of the
+// token-major [B,S,H[i],D] tensor src[i] into the head-major [B,count[i],S,D] buffer dst[i].
+cudaError_t launch_gather_group(const void* const* src, void* const* dst, const int* H,
+                                const int* h0, const int* count, int n, int B, int64_t S, int D,
+                                cudaStream_t stream);
 // dst[b][s][h_begin + h][:] = src[b][h][s][:]
 cudaError_t launch_head_to_seq(const void* src, void* dst, int B, int64_t S, int H, int D,
                                int h_begin, int h_count, cudaStream_t stream);

@@ -7,7 +7,9 @@
 //   * the backward pre-pass: scale * D_i, D_i = <dO_i, O_i> in fp32, the dO gather, the LSE prescale by
 //     log2(e) and the zeroing of the fp32 dQ accumulator, fused in one pass;
 //   * the dQ conversion: fp32 accumulator -> bf16 token-major dq.
-// Each thread moves 16-byte vectors; grids are sized as a multiple of the SM count and loop.
+// Each thread moves 16-byte vectors. Blocks cover fixed runs of sequence positions of one batch
+// row (and head), so no 64-bit division is done per element; the gathers of a head group's
+// Q, K and V go in one launch.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -16,127 +18,175 @@ namespace upipe {
 namespace {
 
 constexpr int kLayoutThreads = 256;
+// Bytes one block of the gather / scatter kernels moves: 32 KiB, 8 16-byte vectors per thread,
+// all loaded before any is stored.
+constexpr int kVecPerThread = 8;
+constexpr int kBlockVecs = kLayoutThreads * kVecPerThread;
 
-inline unsigned grid_for(int64_t work, int threads) {
-  int dev = 0, sms = 152;
-  if (cudaGetDevice(&dev) == cudaSuccess) {
-    int v = 0;
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
-      sms = v;
-  }
-  int64_t blocks = (work + threads - 1) / threads;
-  const int64_t cap = static_cast<int64_t>(sms) * 16;
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
-  return static_cast<unsigned>(blocks);
-}
+// Up to three head-group copies in one launch. Job j moves heads [h0, h0 + count) of a
+// token-major [B, S, H, D] tensor to (or, for the scatter, from) a head-major
+// [B, count, S, D] buffer. A job is cut into blocks of `rows` consecutive sequence positions of
+// one batch row; a block's rows * count * Dc vectors are numbered (row, head, chunk), so the
+// token-major side is contiguous. All index arithmetic inside a block is 32-bit.
+struct LayoutJobs {
+  const uint4* src[3];
+  uint4* dst[3];
+  int H[3], h0[3], count[3];
+  int rows[3];       // sequence positions per block
+  int seq_blocks[3]; // blocks per batch row: ceil(S / rows)
+  int first_block[4];  // prefix sums of the jobs' block counts (B * seq_blocks)
+  int n_jobs;
+};
 
-// One work item = one 16-byte chunk (8 bf16). Items are ordered (b, s, h, chunk) so that the
-// token-major side is read/written contiguously.
-__global__ void seq_to_head_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int B,
-                                   int64_t S, int H, int Dc, int h_begin, int h_count) {
-  const int64_t total = static_cast<int64_t>(B) * S * h_count * Dc;
-  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
-       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int c = static_cast<int>(idx % Dc);
-    int64_t r = idx / Dc;
-    const int h = static_cast<int>(r % h_count);
-    r /= h_count;
-    const int64_t s = r % S;
-    const int64_t b = r / S;
-    const uint4 v = __ldg(src + ((b * S + s) * H + h_begin + h) * Dc + c);
-    dst[((b * h_count + h) * S + s) * Dc + c] = v;
-  }
-}
-
-__global__ void head_to_seq_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int B,
-                                   int64_t S, int H, int Dc, int h_begin, int h_count) {
-  const int64_t total = static_cast<int64_t>(B) * S * h_count * Dc;
-  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
-       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int c = static_cast<int>(idx % Dc);
-    int64_t r = idx / Dc;
-    const int h = static_cast<int>(r % h_count);
-    r /= h_count;
-    const int64_t s = r % S;
-    const int64_t b = r / S;
-    dst[((b * S + s) * H + h_begin + h) * Dc + c] = __ldg(src + ((b * h_count + h) * S + s) * Dc + c);
-  }
-}
-
-// One group of Dc = D/8 consecutive lanes handles one (b, s, h) row; Dc is 8 or 16 and
-// divides the warp, so the row reduction stays inside a warp. o and dout are token-major
-// [B,S,Hq,D] (dout is gathered into dow on the way), or, with head_major_in, this group's
-// head-major [B*hc][S][D] copies (dout then already is dow, which is not written).
-__global__ void bwd_pre_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout,
-                               const float* __restrict__ lse, uint4* __restrict__ dow,
-                               float* __restrict__ dvec, float* __restrict__ lse2,
-                               float4* __restrict__ dqacc, int B, int64_t S, int64_t S_pad, int Hq,
-                               int Dc, int h0, int hc, float scale, int head_major_in) {
-  const int64_t rows = static_cast<int64_t>(B) * S_pad * hc;
-  const int64_t total = rows * Dc;
-  const float kLog2e = 1.4426950408889634f;
-  for (int64_t base = blockIdx.x * static_cast<int64_t>(blockDim.x);
-       base < total; base += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t idx = base + threadIdx.x;
-    const bool live = idx < total;
-    const int c = static_cast<int>(idx % Dc);
-    int64_t r = idx / Dc;
-    const int h = static_cast<int>(r % hc);
-    r /= hc;
-    const int64_t s = r % S_pad;
-    const int64_t b = r / S_pad;
-    float dot = 0.f;
-    const int64_t zrow = (b * hc + h) * S_pad + s;  // row of dvec / lse2 / dqacc
-    if (live) {
-      if (s < S) {
-        const int64_t hm = ((b * hc + h) * S + s) * Dc + c;
-        const int64_t tok = head_major_in ? hm : ((b * S + s) * Hq + h0 + h) * Dc + c;
-        const uint4 ov = __ldg(o + tok);
-        const uint4 dv = __ldg(dout + tok);
-        if (!head_major_in) dow[hm] = dv;
-        const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
-        const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
+template <bool kToHead>
+__global__ void __launch_bounds__(kLayoutThreads)
+    layout_kernel(const LayoutJobs J, int64_t S, int Dc) {
+  int j = 0;
+  while (j + 1 < J.n_jobs && static_cast<int>(blockIdx.x) >= J.first_block[j + 1]) ++j;
+  const int bt = static_cast<int>(blockIdx.x) - J.first_block[j];
+  const int b = bt / J.seq_blocks[j];
+  const int64_t s0 = static_cast<int64_t>(bt - b * J.seq_blocks[j]) * J.rows[j];
+  const int count = J.count[j], W = count * Dc;
+  const int nrows = static_cast<int>(S - s0 < J.rows[j] ? S - s0 : J.rows[j]);
+  const int n = nrows * W;
+  // token-major rows of this block start at (b*S + s0)*H + h0; head-major rows at
+  // (b*count + h)*S + s0
+  const int64_t tok0 = ((static_cast<int64_t>(b) * S + s0) * J.H[j] + J.h0[j]) * Dc;
+  const int64_t tokStride = static_cast<int64_t>(J.H[j]) * Dc;
+  const int64_t hm0 = (static_cast<int64_t>(b) * count * S + s0) * Dc;
+  const int64_t hmStride = S * Dc;
+  const uint4* __restrict__ src = J.src[j];
+  uint4* __restrict__ dst = J.dst[j];
+  uint4 v[kVecPerThread];
+  int64_t to[kVecPerThread];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 a = __bfloat1622float2(o2[i]);
-          const float2 g = __bfloat1622float2(d2[i]);
-          dot = fmaf(a.x, g.x, dot);
-          dot = fmaf(a.y, g.y, dot);
-        }
-      }
-      // zero this chunk's share of the dQ accumulator row (D floats = 2*Dc float4)
-      dqacc[zrow * 2 * Dc + 2 * c] = make_float4(0.f, 0.f, 0.f, 0.f);
-      dqacc[zrow * 2 * Dc + 2 * c + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int u = 0; u < kVecPerThread; ++u) {
+    const int i = static_cast<int>(threadIdx.x) + u * kLayoutThreads;
+    if (i < n) {
+      const int r = i / W, w = i - r * W;
+      const int h = w / Dc, c = w - h * Dc;
+      const int64_t tok = tok0 + r * tokStride + w;
+      const int64_t hm = hm0 + h * hmStride + static_cast<int64_t>(r) * Dc + c;
+      v[u] = __ldg(src + (kToHead ? tok : hm));
+      to[u] = kToHead ? hm : tok;
     }
-    for (int off = Dc / 2; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-    if (live && c == 0) {
+  }
+#pragma unroll
+  for (int u = 0; u < kVecPerThread; ++u) {
+    const int i = static_cast<int>(threadIdx.x) + u * kLayoutThreads;
+    if (i < n) dst[to[u]] = v[u];
+  }
+}
+
+cudaError_t launch_layout(bool to_head, const void* const* src, void* const* dst, const int* H,
+                          const int* h0, const int* count, int n_jobs, int B, int64_t S, int D,
+                          cudaStream_t stream) {
+  const int Dc = D / 8;
+  LayoutJobs J{};
+  J.n_jobs = n_jobs;
+  int64_t total = 0;
+  for (int j = 0; j < n_jobs; ++j) {
+    J.src[j] = static_cast<const uint4*>(src[j]);
+    J.dst[j] = static_cast<uint4*>(dst[j]);
+    J.H[j] = H[j];
+    J.h0[j] = h0[j];
+    J.count[j] = count[j];
+    const int W = count[j] * Dc;
+    J.rows[j] = kBlockVecs / W > 0 ? kBlockVecs / W : 1;
+    const int64_t sb = (S + J.rows[j] - 1) / J.rows[j];
+    if (W > kBlockVecs || sb * B > (int64_t(1) << 30)) return cudaErrorInvalidValue;
+    J.seq_blocks[j] = static_cast<int>(sb);
+    J.first_block[j] = static_cast<int>(total);
+    total += sb * B;
+  }
+  J.first_block[n_jobs] = static_cast<int>(total);
+  if (total > (int64_t(1) << 31) - 1) return cudaErrorInvalidValue;
+  launch_begin(0, stream);
+  if (to_head)
+    layout_kernel<true><<<static_cast<unsigned>(total), kLayoutThreads, 0, stream>>>(J, S, Dc);
+  else
+    layout_kernel<false><<<static_cast<unsigned>(total), kLayoutThreads, 0, stream>>>(J, S, Dc);
+  cudaError_t e = cudaGetLastError();
+  launch_end(0, stream);
+  return e;
+}
+
+// The backward pre-pass. A block covers kPreRows sequence positions of one (batch, head) of
+// the group (grid: position blocks x hc x B); one group of Dc = D/8 consecutive lanes handles
+// one position, so the row reduction stays inside a warp (Dc is 8 or 16). o and dout are
+// token-major [B,S,Hq,D] (dout is gathered into dow on the way), or, with head_major_in, this
+// group's head-major [B*hc][S][D] copies (dout then already is dow, which is not written).
+constexpr int kPreRows = 64;
+
+__global__ void __launch_bounds__(kLayoutThreads)
+    bwd_pre_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout,
+                   const float* __restrict__ lse, uint4* __restrict__ dow,
+                   float* __restrict__ dvec, float* __restrict__ lse2,
+                   float4* __restrict__ dqacc, int64_t S, int64_t S_pad, int Hq, int Dc, int h0,
+                   int hc, float scale, int head_major_in) {
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int per_pass = kLayoutThreads / Dc;  // positions per pass of the block
+  const int c = static_cast<int>(threadIdx.x) % Dc;
+  const int64_t zbase = (static_cast<int64_t>(b) * hc + h) * S_pad;  // dvec / lse2 / dqacc rows
+  const float kLog2e = 1.4426950408889634f;
+  // S_pad is a multiple of 128 and the grid covers it exactly, so every lane of a warp runs
+  // every pass (the shuffles below need all 32).
+  for (int r = static_cast<int>(threadIdx.x) / Dc; r < kPreRows; r += per_pass) {
+    const int64_t s = static_cast<int64_t>(blockIdx.x) * kPreRows + r;
+    float dot = 0.f;
+    if (s < S) {
+      const int64_t hm = ((static_cast<int64_t>(b) * hc + h) * S + s) * Dc + c;
+      const int64_t tok =
+          head_major_in ? hm : ((static_cast<int64_t>(b) * S + s) * Hq + h0 + h) * Dc + c;
+      const uint4 ov = __ldg(o + tok);
+      const uint4 dv = __ldg(dout + tok);
+      if (!head_major_in) dow[hm] = dv;
+      const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+      const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 a = __bfloat1622float2(o2[i]);
+        const float2 g = __bfloat1622float2(d2[i]);
+        dot = fmaf(a.x, g.x, dot);
+        dot = fmaf(a.y, g.y, dot);
+      }
+    }
+    // zero this chunk's share of the dQ accumulator row (D floats = 2*Dc float4)
+    const int64_t zrow = zbase + s;
+    dqacc[zrow * 2 * Dc + 2 * c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    dqacc[zrow * 2 * Dc + 2 * c + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int off = Dc / 2; off > 0; off >>= 1)
+      dot += __shfl_xor_sync(0xffffffffu, dot, off, Dc);
+    if (c == 0) {
       dvec[zrow] = (s < S) ? -(dot * scale) : 0.f;
-      lse2[zrow] = (s < S) ? -(lse[(b * Hq + h0 + h) * S + s] * kLog2e) : 0.f;
+      lse2[zrow] =
+          (s < S) ? -(lse[(static_cast<int64_t>(b) * Hq + h0 + h) * S + s] * kLog2e) : 0.f;
     }
   }
 }
 
 // dq rows hold out_heads heads; this group's go to heads [out_head0, out_head0 + hc): the
-// token-major [B,S,Hq,D] output (Hq, h0) or a group staging [B,S,hc,D] (hc, 0).
-__global__ void dq_convert_kernel(const float4* __restrict__ dqacc, uint4* __restrict__ dq, int B,
-                                  int64_t S, int64_t S_pad, int out_heads, int Dc, int out_head0,
-                                  int hc) {
-  const int64_t total = static_cast<int64_t>(B) * S * hc * Dc;
-  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
-       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int c = static_cast<int>(idx % Dc);
-    int64_t r = idx / Dc;
-    const int h = static_cast<int>(r % hc);
-    r /= hc;
-    const int64_t s = r % S;
-    const int64_t b = r / S;
-    const int64_t zrow = (b * hc + h) * S_pad + s;
-    const float4 x = dqacc[zrow * 2 * Dc + 2 * c];
-    const float4 y = dqacc[zrow * 2 * Dc + 2 * c + 1];
+// token-major [B,S,Hq,D] output (Hq, h0) or a group staging [B,S,hc,D] (hc, 0). A block covers
+// kConvRows positions of one (batch, head) (grid: position blocks x hc x B).
+constexpr int kConvRows = 128;
+
+__global__ void __launch_bounds__(kLayoutThreads)
+    dq_convert_kernel(const float4* __restrict__ dqacc, uint4* __restrict__ dq, int64_t S,
+                      int64_t S_pad, int out_heads, int Dc, int out_head0, int hc) {
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int64_t s0 = static_cast<int64_t>(blockIdx.x) * kConvRows;
+  const int64_t zbase = (static_cast<int64_t>(b) * hc + h) * S_pad + s0;
+  const int64_t obase = (static_cast<int64_t>(b) * S + s0) * out_heads + out_head0 + h;
+  const int n = static_cast<int>((S - s0 < kConvRows ? S - s0 : kConvRows) * Dc);
+  for (int i = static_cast<int>(threadIdx.x); i < n; i += kLayoutThreads) {
+    const int r = i / Dc, c = i - r * Dc;
+    const int64_t z = (zbase + r) * 2 * Dc + 2 * c;
+    const float4 x = dqacc[z];
+    const float4 y = dqacc[z + 1];
     __nv_bfloat162 w[4] = {__floats2bfloat162_rn(x.x, x.y), __floats2bfloat162_rn(x.z, x.w),
                            __floats2bfloat162_rn(y.x, y.y), __floats2bfloat162_rn(y.z, y.w)};
-    dq[((b * S + s) * out_heads + out_head0 + h) * Dc + c] = *reinterpret_cast<const uint4*>(w);
+    dq[(obase + static_cast<int64_t>(r) * out_heads) * Dc + c] =
+        *reinterpret_cast<const uint4*>(w);
   }
 }
 
@@ -144,26 +194,22 @@ __global__ void dq_convert_kernel(const float4* __restrict__ dqacc, uint4* __res
 
 cudaError_t launch_seq_to_head(const void* src, void* dst, int B, int64_t S, int H, int D,
                                int h_begin, int h_count, cudaStream_t stream) {
-  const int Dc = D / 8;
-  const int64_t work = static_cast<int64_t>(B) * S * h_count * Dc;
-  launch_begin(0, stream);
-  seq_to_head_kernel<<<grid_for(work, kLayoutThreads), kLayoutThreads, 0, stream>>>(
-      static_cast<const uint4*>(src), static_cast<uint4*>(dst), B, S, H, Dc, h_begin, h_count);
-  cudaError_t e = cudaGetLastError();
-  launch_end(0, stream);
-  return e;
+  return launch_layout(true, &src, &dst, &H, &h_begin, &h_count, 1, B, S, D, stream);
+}
+
+cudaError_t launch_gather_group(const void* const* src, void* const* dst, const int* H,
+                                const int* h0, const int* count, int n, int B, int64_t S, int D,
+                                cudaStream_t stream) {
+  if (n < 1 || n > 3) return cudaErrorInvalidValue;
+  return launch_layout(true, src, dst, H, h0, count, n, B, S, D, stream);
 }
 
 cudaError_t launch_head_to_seq(const void* src, void* dst, int B, int64_t S, int H, int D,
                                int h_begin, int h_count, cudaStream_t stream) {
-  const int Dc = D / 8;
-  const int64_t work = static_cast<int64_t>(B) * S * h_count * Dc;
-  launch_begin(0, stream);
-  head_to_seq_kernel<<<grid_for(work, kLayoutThreads), kLayoutThreads, 0, stream>>>(
-      static_cast<const uint4*>(src), static_cast<uint4*>(dst), B, S, H, Dc, h_begin, h_count);
-  cudaError_t e = cudaGetLastError();
-  launch_end(0, stream);
-  return e;
+  void* dsts[1] = {dst};
+  const void* srcs[1] = {src};
+  // the same job description, read the other way: head-major source, token-major destination
+  return launch_layout(false, srcs, dsts, &H, &h_begin, &h_count, 1, B, S, D, stream);
 }
 
 cudaError_t launch_bwd_pre(const void* o, const void* dout, const float* lse, void* dow,
@@ -171,11 +217,12 @@ cudaError_t launch_bwd_pre(const void* o, const void* dout, const float* lse, vo
                            int64_t S_pad, int Hq, int D, int h0, int hc, float scale,
                            int head_major_in, cudaStream_t stream) {
   const int Dc = D / 8;
-  const int64_t work = static_cast<int64_t>(B) * S_pad * hc * Dc;
+  const dim3 grid(static_cast<unsigned>((S_pad + kPreRows - 1) / kPreRows),
+                  static_cast<unsigned>(hc), static_cast<unsigned>(B));
   launch_begin(2, stream);
-  bwd_pre_kernel<<<grid_for(work, kLayoutThreads), kLayoutThreads, 0, stream>>>(
+  bwd_pre_kernel<<<grid, kLayoutThreads, 0, stream>>>(
       static_cast<const uint4*>(o), static_cast<const uint4*>(dout), lse,
-      static_cast<uint4*>(dow), dvec, lse2, reinterpret_cast<float4*>(dqacc), B, S, S_pad, Hq, Dc,
+      static_cast<uint4*>(dow), dvec, lse2, reinterpret_cast<float4*>(dqacc), S, S_pad, Hq, Dc,
       h0, hc, scale, head_major_in);
   cudaError_t e = cudaGetLastError();
   launch_end(2, stream);
@@ -185,10 +232,11 @@ cudaError_t launch_bwd_pre(const void* o, const void* dout, const float* lse, vo
 cudaError_t launch_dq_convert(const float* dqacc, void* dq, int B, int64_t S, int64_t S_pad,
                               int out_heads, int D, int out_head0, int hc, cudaStream_t stream) {
   const int Dc = D / 8;
-  const int64_t work = static_cast<int64_t>(B) * S * hc * Dc;
+  const dim3 grid(static_cast<unsigned>((S + kConvRows - 1) / kConvRows),
+                  static_cast<unsigned>(hc), static_cast<unsigned>(B));
   launch_begin(4, stream);
-  dq_convert_kernel<<<grid_for(work, kLayoutThreads), kLayoutThreads, 0, stream>>>(
-      reinterpret_cast<const float4*>(dqacc), static_cast<uint4*>(dq), B, S, S_pad, out_heads, Dc,
+  dq_convert_kernel<<<grid, kLayoutThreads, 0, stream>>>(
+      reinterpret_cast<const float4*>(dqacc), static_cast<uint4*>(dq), S, S_pad, out_heads, Dc,
       out_head0, hc);
   cudaError_t e = cudaGetLastError();
   launch_end(4, stream);

@@ -270,6 +270,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 
+// Returns x through an empty volatile asm: the compiler must treat the result as a new value at
+// each call, so expressions built from it are evaluated where they are used instead of being
+// precomputed (and held in registers) ahead of a loop.
+__device__ __forceinline__ uint64_t opaque_u64(uint64_t x) {
+  asm volatile("" : "+l"(x));
+  return x;
+}
+
 // ---- shared-memory matrix descriptors (tcgen05 format) ------------------------------------
 // Tiles are bf16, 128-byte swizzled, made of "boxes" of 128 rows x 64 elements (16 KiB,
 // 1024-byte aligned), the layout a TMA load with CU_TENSOR_MAP_SWIZZLE_128B and a 64-element

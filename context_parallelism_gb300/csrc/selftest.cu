@@ -137,13 +137,9 @@ cudaError_t launch_selftest_umma(const void* a, const void* b, float* c, int N, 
   if (e != cudaSuccess) return e;
   e = make_tmap_bf16(&tb, b, 128, 128, 1);
   if (e != cudaSuccess) return e;
-  static bool attr_done = false;
-  if (!attr_done) {
-    e = cudaFuncSetAttribute(selftest_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             StSmemLayout::kBytes);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  e = ensure_smem_attr(reinterpret_cast<const void*>(&selftest_umma_kernel),
+                       StSmemLayout::kBytes);
+  if (e != cudaSuccess) return e;
   launch_begin(5, stream);
   selftest_umma_kernel<<<1, kStThreads, StSmemLayout::kBytes, stream>>>(
       ta, tb, static_cast<const __nv_bfloat16*>(a), c, N, K, a_mn, b_mn, a_manual, lbo, sbo,

@@ -427,6 +427,7 @@ int upipe_ce_fwd(const void* h, const void* w, const int64_t* target, float* los
   if (workspace_bytes < p.f_total)
     return lfail(UPIPE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes,
                  p.f_total);
+  const DeviceGuard dguard;
   LOSS_CUDA(cudaSetDevice(dev));
   uint32_t* err = nullptr;
   st = device_status_word(dev, &err);
@@ -480,6 +481,7 @@ int upipe_ce_bwd(const void* h, const void* w, const int64_t* target, const floa
   if (workspace_bytes < p.b_total)
     return lfail(UPIPE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes,
                  p.b_total);
+  const DeviceGuard dguard;
   LOSS_CUDA(cudaSetDevice(dev));
   uint32_t* err = nullptr;
   st = device_status_word(dev, &err);
@@ -561,6 +563,7 @@ int upipe_ce_fwd_bwd(const void* h, const void* w, const int64_t* target, const 
   if (workspace_bytes < p.x_total)
     return lfail(UPIPE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes,
                  p.x_total);
+  const DeviceGuard dguard;
   LOSS_CUDA(cudaSetDevice(dev));
   uint32_t* err = nullptr;
   st = device_status_word(dev, &err);
@@ -662,6 +665,7 @@ int upipe_mlp_fwd(const void* x, const void* w_gu, const void* w_d, void* y, int
   if (workspace_bytes < p.f_total)
     return lfail(UPIPE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes,
                  p.f_total);
+  const DeviceGuard dguard;
   LOSS_CUDA(cudaSetDevice(dev));
   uint32_t* err = nullptr;
   st = device_status_word(dev, &err);
@@ -724,6 +728,7 @@ int upipe_mlp_bwd(const void* x, const void* w_gu, const void* w_d, const void* 
   if (workspace_bytes < p.b_total)
     return lfail(UPIPE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes,
                  p.b_total);
+  const DeviceGuard dguard;
   LOSS_CUDA(cudaSetDevice(dev));
   uint32_t* err = nullptr;
   st = device_status_word(dev, &err);

@@ -24,16 +24,16 @@
  *   - bf16 tensors are passed as `void*` / `const void*` to bf16 (IEEE bfloat16) data.
  *   - Token-major layouts: q, o, dout, dq are [B, S, Hq, D]; k, v, dk, dv are [B, S, Hkv, D],
  *     all dense row-major. lse is float32 [B, Hq, S], natural log.
- *   - Every pointer must be 16-byte aligned. Device pointers must belong to the device that
- *     is current for the caller; k and v may instead both be PINNED host memory
+ *   - Every pointer must be 16-byte aligned. The device pointers of one call must all belong
+ *     to one device; k and v may instead both be PINNED host memory
  *     (cudaHostAlloc / cudaHostRegister), which selects the staged host-K/V path.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream). All work is enqueued on it
  *     and calls return before the GPU finishes (asynchronous, like a kernel launch).
- *   - Devices: one process drives one GPU (one process per GPU under torchrun). Each kernel's
- *     shared-memory size attribute is set once per process, on the device of the first call.
- *     Calling the library on a second GPU from the same process is untested: where the
- *     attribute does not carry over, launches needing more than 48 KiB of shared memory fail
- *     there with UPIPE_ERR_CUDA (an error, not a fault).
+ *   - Devices: each call runs on the device its device tensors belong to, and leaves the
+ *     caller's current device as it found it. Per-device state (copy streams, status word,
+ *     each kernel's shared-memory size attribute) is created on the first call that uses that
+ *     device, under one library lock, so one process may drive several GPUs; the usual
+ *     deployment is one process per GPU (torchrun).
  *   - Ownership: the caller owns every buffer, including the workspace. Per call the library
  *     allocates no device memory. Per device it lazily creates two internal copy streams for
  *     the attention calls and two for the sequence-tiled calls (used only when activations
@@ -155,10 +155,16 @@ int upipe_attn_bwd(const void* q, const void* k, const void* v, const void* o,
  *     stream capture.
  *   - Every call shares the one array, which keeps the last call's contents. Calls whose GPU
  *     work overlaps (different streams, or unordered host threads) race on it: serialise them.
- *   - Arguments as upipe_attn_fwd, except that k and v must be device memory and there is no
- *     workspace. check_status != 0 first synchronises `stream` and returns UPIPE_ERR_TIMEOUT if
- *     a kernel of an earlier call of this function gave up on a bounded wait (blocking; pass 0
- *     to enqueue without waiting).
+ *   - Arguments as upipe_attn_fwd with two restrictions and no workspace: q, k, v, o and lse
+ *     must all be non-null device memory of one device (no pinned-host staging, and no
+ *     prefill form with lse = NULL), else UPIPE_ERR_INVALID_ARG. Shape errors return the same
+ *     status as upipe_attn_fwd (UPIPE_ERR_INVALID_ARG or UPIPE_ERR_UNSUPPORTED), checked
+ *     before any device access. The result is bitwise the one upipe_attn_fwd gives for the
+ *     same arguments with device-resident tensors (same kernels, same arena layout).
+ *   - check_status != 0 first synchronises `stream` and returns UPIPE_ERR_TIMEOUT if a kernel
+ *     of an earlier call of this function gave up on a bounded wait (blocking; pass 0 to
+ *     enqueue without waiting).
+ *   - The caller's current device is left as it was.
  */
 int upipe_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
                            int B, int64_t S, int Hq, int Hkv, int D, int causal, int head_chunk,
@@ -293,7 +299,10 @@ enum {
   UPIPE_K_OTHER = 5,      /* self-tests */
   UPIPE_K_LOSS_GEMM = 6,  /* sequence-tiled loss and MLP: tensor-core GEMMs + epilogues */
   UPIPE_K_LOSS_MERGE = 7, /* sequence-tiled loss: per-token merge, stored logits -> dlogits */
-  UPIPE_K_COUNT = 8
+  UPIPE_K_KV_H2D = 8,     /* not a kernel: one key/value trunk staged host -> device (copy
+                             stream; "launches" counts trunks) */
+  UPIPE_K_DKDV_D2H = 9,   /* not a kernel: one trunk's dK/dV copied device -> host */
+  UPIPE_K_COUNT = 10
 };
 
 typedef struct {
@@ -317,8 +326,11 @@ uint64_t upipe_launch_count(void);
 
 /*
  * Profiling: while enabled, every launch is bracketed by CUDA events recorded on the stream
- * it is launched on. upipe_profile_read() synchronises those events, adds their elapsed
- * times into out[0..n) (indexed by kernel class) and forgets them. Returns a status code.
+ * it is launched on, and so is each key/value trunk staged in (UPIPE_K_KV_H2D) and each
+ * trunk's dK/dV copied out (UPIPE_K_DKDV_D2H) on the library's copy stream.
+ * upipe_profile_read() synchronises those events, adds their elapsed times into out[0..n)
+ * (indexed by class) and forgets them. Returns a status code. Copies are not counted by
+ * upipe_launch_count().
  */
 int upipe_profile_enable(int on);
 int upipe_profile_read(upipe_kernel_stat* out, int n);

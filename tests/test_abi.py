@@ -41,14 +41,12 @@ def _expected_ws(B, S, Hq, Hkv, D, hc, T, kv_host, act_host=False):
     kc = hc // G
     T = min(T, S)
     S_pad = (S + 127) // 128 * 128
-    T_pad = (T + 127) // 128 * 128
     ntr = (S + T - 1) // T
     qw = B * hc * S * D * 2
     kv = 4 * al(B * kc * T * D * 2) if kv_host else 2 * al(B * kc * S * D * 2)
     fwd = al(qw) + kv + (3 * al(qw) if act_host else 0)  # host q/o: Q buffer 2, 2 O stagings
-    if ntr > 1:  # running state: every query trunk's rows with host K/V, one trunk's otherwise
-        rows = S_pad if kv_host else T_pad
-        fwd += al(B * hc * rows * D * 4) + al(B * hc * rows * 8)
+    if kv_host and ntr > 1:  # running state of every query trunk, kept between launches
+        fwd += al(B * hc * S_pad * D * 4) + al(B * hc * S_pad * 8)
     # host K/V: the backward also holds two dK and two dV trunk slots (used when dk/dv are
     # pinned host memory as well)
     dkdv = 4 * al(B * kc * T * D * 2) if kv_host else 0
@@ -279,3 +277,44 @@ def test_fused_loss_workspace_matches_formula(S, Dm, V, T):
     # the attention and MLP workspaces have no fused pass
     assert up.upipe_workspace_bytes(1, 1024, 8, 2, 128, 1, 4, 1024, up.UPIPE_PASS_FUSED) == 0
     assert up.upipe_mlp_workspace_bytes(S, Dm, 128, T, up.UPIPE_PASS_FUSED) == 0
+
+
+# ---- the forward without allocation ----------------------------------------------------------
+
+@pytest.mark.parametrize("args,status", [
+    ((1, 512, 6, 4, 64, 1, 6, 512), up.UPIPE_ERR_INVALID_ARG),      # Hq % Hkv
+    ((1, 512, 32, 8, 128, 1, 2, 512), up.UPIPE_ERR_INVALID_ARG),    # head_chunk % (Hq/Hkv)
+    ((1, 1024, 4, 4, 64, 1, 4, 300), up.UPIPE_ERR_INVALID_ARG),     # seq_trunk % 128
+    ((1, 512, 4, 4, 64, 2, 4, 512), up.UPIPE_ERR_INVALID_ARG),      # causal not 0/1
+    ((1, 512, 4, 4, 96, 1, 4, 512), up.UPIPE_ERR_UNSUPPORTED),      # D
+    ((1, (1 << 30) + 128, 4, 4, 64, 1, 4, 512), up.UPIPE_ERR_UNSUPPORTED),  # S > 2^30
+    ((1, 16384, 32, 8, 128, 1, 32, 16384), up.UPIPE_ERR_WORKSPACE_TOO_SMALL),  # > 32 MiB
+])
+def test_noalloc_status_codes_without_device_access(args, status):
+    """The no-allocation forward validates shapes with the same plan as upipe_attn_fwd and
+    returns the same status for the same bad shape, before touching any pointer; a problem
+    too large for its static scratch is rejected before any device access too."""
+    B, S, Hq, Hkv, D, causal, hc, T = args
+    n0 = up.upipe_launch_count()
+    st = up._lib.upipe_attn_fwd_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, B, S, Hq, Hkv, D, causal,
+                                        hc, T, 0, None)
+    assert st == status, up.upipe_last_error_message()
+    msg = up.upipe_last_error_message()
+    assert msg
+    if status != up.UPIPE_ERR_WORKSPACE_TOO_SMALL:
+        st2 = up._lib.upipe_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, B, S, Hq, Hkv, D, causal, hc,
+                                     T, FAKE, 1 << 40, None)
+        assert st2 == st
+        assert up.upipe_last_error_message() == msg
+    else:
+        assert "32 MiB" in msg
+    assert up.upipe_launch_count() == n0
+
+
+def test_noalloc_rejects_null_and_misaligned_pointers():
+    args = (1, 512, 4, 4, 64, 1, 4, 512)
+    for ptrs in ((FAKE, FAKE, FAKE, FAKE, None),          # no prefill form: lse required
+                 (None, FAKE, FAKE, FAKE, FAKE),
+                 (FAKE, FAKE, FAKE + 8, FAKE, FAKE)):    # v not 16-byte aligned
+        st = up._lib.upipe_attn_fwd_noalloc(*ptrs, *args, 0, None)
+        assert st == up.UPIPE_ERR_INVALID_ARG
