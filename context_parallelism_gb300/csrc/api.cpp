@@ -180,10 +180,9 @@ cudaError_t ensure_smem_attr(const void* kernel, int bytes) {
 namespace {
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
-}  // namespace
 
-cudaError_t make_tmap_bf16(CUtensorMap* map, const void* base, int64_t cols, int64_t rows,
-                           int64_t depth, int box_rows) {
+// The driver's tensor-map encoder, looked up once.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   std::call_once(g_encode_once, [] {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -192,6 +191,13 @@ cudaError_t make_tmap_bf16(CUtensorMap* map, const void* base, int64_t cols, int
         q == cudaDriverEntryPointSuccess)
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   });
+  return g_encode;
+}
+}  // namespace
+
+cudaError_t make_tmap_bf16(CUtensorMap* map, const void* base, int64_t cols, int64_t rows,
+                           int64_t depth, int box_rows) {
+  tensor_map_encoder();
   if (!g_encode) return cudaErrorNotSupported;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
                               static_cast<cuuint64_t>(depth)};
@@ -297,6 +303,17 @@ int make_attn_plan(int B, int64_t S, int Hq, int Hkv, int D, int causal, int hea
   p->b_dqacc = take(hcB * p->S_pad * D * 4);
   p->b_lse2 = take(hcB * p->S_pad * 4);
   p->b_dvec = take(hcB * p->S_pad * 4);
+  // Short causal sequences: a key tile's backward walk covers the query tiles of all G q-heads
+  // of its kv-head, and the earliest key tiles walk the most, so with few key tiles per launch
+  // the first CTAs set the launch time (at S = 8K and 2 kv-heads: 128 CTAs, the longest 64
+  // times the shortest). Up to S = 16K the walk is shared by G CTAs, one q-head each, whose
+  // fp32 dK/dV shares a reduce kernel adds in a fixed order. The rule depends on the shape
+  // only (not on head_chunk), so the workspace stays proportional to head_chunk.
+  if (causal && D == 128 && G > 1 && S <= 16384) {
+    p->bwd_split = G;
+    p->part_rows = p->kv_host ? p->T_pad : p->S_pad;
+    p->b_dkv_part = take(static_cast<size_t>(G) * kcB * p->part_rows * 2 * D * 4);
+  }
   p->b_total = off;
   return UPIPE_OK;
 }
@@ -907,7 +924,14 @@ int upipe_attn_bwd(const void* q, const void* k, const void* v, const void* o, c
       } else {
         a.kv_row_lo = t0; a.kv_row_hi = t0 + Tn; a.kv_pos0 = 0;
       }
+      a.split = p.bwd_split;
+      a.dkv_part = p.bwd_split > 1 ? reinterpret_cast<float*>(ws + p.b_dkv_part) : nullptr;
+      a.part_rows = p.part_rows;
       UPIPE_CUDA(launch_attn_bwd(D, B, tq, tdo, tk, tv, a, stream));
+      if (p.bwd_split > 1)
+        UPIPE_CUDA(launch_dkdv_reduce(a.dkv_part, p.bwd_split, p.part_rows, Tn, t0, B, p.kc, D,
+                                      S, a.dk, a.dv, a.dkv_rows, a.dkv_row0, a.dkv_heads,
+                                      a.dkv_head0, stream));
       if (kv_host) {
         st = stg.after(job);
         if (st != UPIPE_OK) return st;

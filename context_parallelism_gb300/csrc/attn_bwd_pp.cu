@@ -22,11 +22,14 @@
 // to S columns [64w, 64w+32) (inside the columns it alone reads), and its dS^T to shared box w.
 // A third warpgroup drains dQ^T(i) from TMEM into the fp32 accumulator, off the groups' path.
 //
-// MMA issue order: S(0), dV(0), dP(0), then per tile i: S(i+1), dQ(i), dK(i), dV(i+1), dP(i+1).
-// Each group runs dS(i) then P(i+1), so its dS(i) overlaps S(i+1) and its P(i+1) overlaps dQ(i)
-// and dK(i); the drain reads dQ(i) while dK(i) and dV(i+1) run (dQ goes first for that). One thread's MMAs execute in order, so
-// S(i+1) overwrites S only after dV(i) has read P^T(i), and the commit that publishes dP(i+1)
-// also covers dK(i) and dQ(i), which read the single dS^T buffer the groups then overwrite.
+// MMA issue order: S(0), dP(0), dV(0), then per tile i: S(i+1), dQ(i), dK(i), dP(i+1), dV(i+1).
+// Each group runs dS(i) then P(i+1): its dS(i) overlaps S(i+1), and its P(i+1) overlaps dQ(i),
+// dK(i) and dP(i+1), so dP(i+1) is ready when the group turns to dS(i+1) (issued before dV(i+1),
+// which must wait for P(i+1)). The drain reads dQ(i) while dK(i) runs (dQ goes first for that)
+// and releases the columns dP(i+1) reuses. One thread's MMAs execute in order, so S(i+1)
+// overwrites S only after dV(i) has read P^T(i); the commit that publishes dP(i+1) also covers
+// dK(i) and dQ(i), which read the single dS^T buffer the groups then overwrite; and the commit
+// that frees a dO stage (after dV(i+1)) covers dP(i+1), its other reader.
 //
 // Threads (512): warps 0-3 compute group 0, warps 4-7 compute group 1, warps 8-11 dQ drain,
 // warp 12 TMEM + MMA issue, warp 13 TMA producer, warps 14-15 idle. Registers move from the
@@ -105,7 +108,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int kt = blockIdx.x;  // smallest key positions (most query tiles) first
-  const int kvl = blockIdx.y;
+  const int split = a.split > 1 ? a.split : 1;
+  const int kvl = static_cast<int>(blockIdx.y) / split;
+  const int sp = static_cast<int>(blockIdx.y) - kvl * split;  // share of the group's q-heads
+  const int gh = a.G / split;                                 // q-heads this CTA walks
   const int b = blockIdx.z;
   const int64_t r0 = a.kv_row_lo + static_cast<int64_t>(kt) * 128;  // K/V map row
   const int64_t p0 = a.kv_pos0 + r0;                                // global key position
@@ -113,7 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int qt_lo = a.causal ? static_cast<int>(p0 / 128) : 0;
   const int qt_hi = static_cast<int>((a.S + 127) / 128);
   const int nq = qt_hi > qt_lo ? qt_hi - qt_lo : 0;
-  const int n_it = a.G * nq;
+  const int n_it = gh * nq;
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -161,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
   auto decode = [&](const Cursor& c, int& zq, int64_t& q0) {
-    zq = b * a.hc + kvl * a.G + c.head;
+    zq = b * a.hc + kvl * a.G + sp * gh + c.head;
     q0 = static_cast<int64_t>(qt_lo + c.qt) * 128;
   };
 
@@ -297,11 +303,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
 
-      if (ok && n_it > 0) ok = issue_s(0) && issue_dv(0) && issue_dp(0);
+      if (ok && n_it > 0) ok = issue_s(0) && issue_dp(0) && issue_dv(0);
       for (int i = 0; ok && i < n_it; ++i) {
         if (i + 1 < n_it && !issue_s(i + 1)) { ok = false; break; }
         if (!issue_dk_dq(i)) { ok = false; break; }
-        if (i + 1 < n_it && !(issue_dv(i + 1) && issue_dp(i + 1))) { ok = false; break; }
+        if (i + 1 < n_it && !(issue_dp(i + 1) && issue_dv(i + 1))) { ok = false; break; }
       }
       if (ok) {
         umma_commit(done);
@@ -450,7 +456,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       good = __all_sync(0xffffffffu, wait(done, 0));
       if (good) tc_fence_after();
     }
-    if (good) {
+    if (good && split > 1) {
+      // this CTA's fp32 share of dV (group 0) or dK (group 1) for its key rows; the reduce
+      // kernel adds the shares of the key tile's CTAs in a fixed order
+      const uint32_t tAcc = w == 0 ? tDV : tDK;
+      float* part = a.dkv_part +
+                    (((static_cast<int64_t>(sp) * gridDim.z + b) * a.kc + kvl) * a.part_rows +
+                     (r0 - a.kv_row_lo) + t) * (2 * kD) + (w == 0 ? kD : 0);
+#pragma unroll
+      for (int c = 0; c < kD / 32; ++c) {
+        uint32_t r[32];
+        if (n_it > 0) {
+          tmem_ld32_sync(tAcc + lane_off + c * 32, r);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = 0u;
+        }
+#pragma unroll
+        for (int i = 0; i < 32; i += 4)
+          *reinterpret_cast<float4*>(part + c * 32 + i) =
+              make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
+                          __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+      }
+    } else if (good) {
       // group 0 writes dV, group 1 writes dK (both already carry their final scaling)
       const uint32_t tAcc = w == 0 ? tDV : tDK;
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(w == 0 ? a.dv : a.dk) +
@@ -505,7 +533,11 @@ cudaError_t launch_attn_bwd(int D, int B, const CUtensorMap& q_map, const CUtens
     if (e != cudaSuccess) return e;
   }
   const int64_t n_kt = (a.kv_row_hi - a.kv_row_lo + 127) / 128;
-  dim3 grid(static_cast<unsigned>(n_kt), static_cast<unsigned>(a.kc), static_cast<unsigned>(B));
+  const int split = a.split > 1 ? a.split : 1;
+  if (a.G % split || (split > 1 && (!a.dkv_part || a.part_rows < n_kt * 128)))
+    return cudaErrorInvalidValue;
+  dim3 grid(static_cast<unsigned>(n_kt), static_cast<unsigned>(a.kc * split),
+            static_cast<unsigned>(B));
   launch_begin(3, stream);
   attn_bwd_pp_kernel<<<grid, kThreads, BppLayout::kBytes, stream>>>(q_map, do_map, k_map, v_map, a);
   cudaError_t e = cudaGetLastError();

@@ -46,6 +46,11 @@ struct AttnPlan {
   // host activations: second Q and dO buffers, head-major O copies, dQ output stagings
   size_t b_qw2 = 0, b_dow2 = 0, b_ow[2] = {0, 0}, b_dqs[2] = {0, 0};
   size_t b_dqacc = 0, b_lse2 = 0, b_dvec = 0, b_total = 0;
+  // Split backward (short causal sequences, see make_attn_plan): each key tile's walk is shared
+  // by bwd_split CTAs, whose fp32 dK/dV shares of part_rows key rows live at b_dkv_part.
+  int bwd_split = 1;
+  int64_t part_rows = 0;
+  size_t b_dkv_part = 0;
 };
 
 
@@ -152,6 +157,14 @@ struct BwdArgs {
   void* dv;
   int64_t dkv_rows, dkv_row0;
   int dkv_heads, dkv_head0;
+  // split > 1 (a divisor of G): each key tile's walk is shared by `split` CTAs, CTA sp taking
+  // q-heads [sp*G/split, (sp+1)*G/split) of the group; each writes its fp32 dK, dV share of
+  // key row r (launch-relative, r = p - kv_pos0 - kv_row_lo) to
+  // dkv_part + (((sp * B + b) * kc + kvl) * part_rows + r) * 2 * D, dK in the first D floats,
+  // dV in the next, and launch_dkdv_reduce adds the shares up. split = 1: dk, dv as above.
+  int split;
+  float* dkv_part;
+  int64_t part_rows;
   uint32_t* err;
 };
 
@@ -191,6 +204,15 @@ cudaError_t launch_bwd_pre(const void* o, const void* dout, const float* lse, vo
                            float* dvec, float* lse2, float* dqacc, int B, int64_t S,
                            int64_t S_pad, int Hq, int D, int h0, int hc, float scale,
                            int head_major_in, cudaStream_t stream);
+
+// Sums the split backward's shares (BwdArgs::split, dkv_part) of key rows [0, rows) in order
+// sp = 0, 1, ... and writes them as bf16 with the epilogue's addressing: element (b, row r,
+// kv-head kvl, d) of dK goes to dk[((b * dkv_rows + row0_pos + r - dkv_row0) * dkv_heads +
+// dkv_head0 + kvl) * D + d], dV likewise; rows with row0_pos + r >= S are skipped.
+cudaError_t launch_dkdv_reduce(const float* part, int split, int64_t part_rows, int64_t rows,
+                               int64_t row0_pos, int B, int kc, int D, int64_t S, void* dk,
+                               void* dv, int64_t dkv_rows, int64_t dkv_row0, int dkv_heads,
+                               int dkv_head0, cudaStream_t stream);
 
 // dq[b][s][h0+h][:] = bf16(dqacc[(b*hc+h)*S_pad + s][:])
 // dq rows of out_heads heads, this group's at [out_head0, out_head0 + hc): (Hq, h0) for the

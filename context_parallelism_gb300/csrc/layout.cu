@@ -39,11 +39,10 @@ struct LayoutJobs {
 };
 
 template <bool kToHead>
-__global__ void __launch_bounds__(kLayoutThreads)
-    layout_kernel(const LayoutJobs J, int64_t S, int Dc) {
+__device__ __forceinline__ void layout_task(const LayoutJobs& J, int64_t S, int Dc, int task) {
   int j = 0;
-  while (j + 1 < J.n_jobs && static_cast<int>(blockIdx.x) >= J.first_block[j + 1]) ++j;
-  const int bt = static_cast<int>(blockIdx.x) - J.first_block[j];
+  while (j + 1 < J.n_jobs && task >= J.first_block[j + 1]) ++j;
+  const int bt = task - J.first_block[j];
   const int b = bt / J.seq_blocks[j];
   const int64_t s0 = static_cast<int64_t>(bt - b * J.seq_blocks[j]) * J.rows[j];
   const int count = J.count[j], W = count * Dc;
@@ -78,6 +77,14 @@ __global__ void __launch_bounds__(kLayoutThreads)
   }
 }
 
+template <bool kToHead>
+__global__ void __launch_bounds__(kLayoutThreads)
+    layout_kernel(const LayoutJobs J, int64_t S, int Dc) {
+  // A fixed grid of a few blocks per SM loops over the block tasks (no block turnover).
+  for (int task = blockIdx.x; task < J.first_block[J.n_jobs]; task += gridDim.x)
+    layout_task<kToHead>(J, S, Dc, task);
+}
+
 cudaError_t launch_layout(bool to_head, const void* const* src, void* const* dst, const int* H,
                           const int* h0, const int* count, int n_jobs, int B, int64_t S, int D,
                           cudaStream_t stream) {
@@ -101,11 +108,16 @@ cudaError_t launch_layout(bool to_head, const void* const* src, void* const* dst
   }
   J.first_block[n_jobs] = static_cast<int>(total);
   if (total > (int64_t(1) << 31) - 1) return cudaErrorInvalidValue;
+  int dev = 0, sms = 152;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // 8 resident blocks of 256 threads per SM
+  const unsigned grid = static_cast<unsigned>(total < 8LL * sms ? total : 8LL * sms);
   launch_begin(0, stream);
   if (to_head)
-    layout_kernel<true><<<static_cast<unsigned>(total), kLayoutThreads, 0, stream>>>(J, S, Dc);
+    layout_kernel<true><<<grid, kLayoutThreads, 0, stream>>>(J, S, Dc);
   else
-    layout_kernel<false><<<static_cast<unsigned>(total), kLayoutThreads, 0, stream>>>(J, S, Dc);
+    layout_kernel<false><<<grid, kLayoutThreads, 0, stream>>>(J, S, Dc);
   cudaError_t e = cudaGetLastError();
   launch_end(0, stream);
   return e;
@@ -190,6 +202,44 @@ __global__ void __launch_bounds__(kLayoutThreads)
   }
 }
 
+// Split backward: the shares of `split` CTAs per key tile, added in a fixed order. One thread
+// per 16-byte output vector (8 bf16 of dK or dV); a block covers kRedRows key rows of one
+// (batch, kv-head) (grid: row blocks x kc x B).
+constexpr int kRedRows = 64;
+
+__global__ void __launch_bounds__(kLayoutThreads)
+    dkdv_reduce_kernel(const float4* __restrict__ part, int split, int64_t part_rows,
+                       int64_t rows, int64_t row0_pos, int B, int kc, int Dc, int64_t S,
+                       uint4* __restrict__ dk, uint4* __restrict__ dv, int64_t dkv_rows,
+                       int64_t dkv_row0, int dkv_heads, int dkv_head0) {
+  const int kvl = blockIdx.y, b = blockIdx.z;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kRedRows;
+  const int per_row = 2 * Dc;  // dK's Dc vectors, then dV's
+  const int n = static_cast<int>((rows - r0 < kRedRows ? rows - r0 : kRedRows) * per_row);
+  const int64_t slot = static_cast<int64_t>(B) * kc * part_rows * 2 * Dc * 2;  // float4s
+  for (int i = static_cast<int>(threadIdx.x); i < n; i += kLayoutThreads) {
+    const int rr = i / per_row, v = i - rr * per_row;
+    const int64_t r = r0 + rr;
+    const int64_t pos = row0_pos + r;
+    if (pos >= S) continue;
+    // float4 index of the share's 8 floats: row (b, kvl, r), vector v of its 2D floats
+    const int64_t f = ((static_cast<int64_t>(b) * kc + kvl) * part_rows + r) * (4 * Dc) + 2 * v;
+    float4 x = part[f], y = part[f + 1];
+    for (int sp = 1; sp < split; ++sp) {
+      const float4 x2 = part[sp * slot + f], y2 = part[sp * slot + f + 1];
+      x.x += x2.x; x.y += x2.y; x.z += x2.z; x.w += x2.w;
+      y.x += y2.x; y.y += y2.y; y.z += y2.z; y.w += y2.w;
+    }
+    __nv_bfloat162 o[4] = {__floats2bfloat162_rn(x.x, x.y), __floats2bfloat162_rn(x.z, x.w),
+                           __floats2bfloat162_rn(y.x, y.y), __floats2bfloat162_rn(y.z, y.w)};
+    const bool is_v = v >= Dc;
+    const int c = is_v ? v - Dc : v;
+    uint4* out = is_v ? dv : dk;
+    out[((static_cast<int64_t>(b) * dkv_rows + pos - dkv_row0) * dkv_heads + dkv_head0 + kvl) *
+            Dc + c] = *reinterpret_cast<const uint4*>(o);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_seq_to_head(const void* src, void* dst, int B, int64_t S, int H, int D,
@@ -238,6 +288,23 @@ cudaError_t launch_dq_convert(const float* dqacc, void* dq, int B, int64_t S, in
   dq_convert_kernel<<<grid, kLayoutThreads, 0, stream>>>(
       reinterpret_cast<const float4*>(dqacc), static_cast<uint4*>(dq), S, S_pad, out_heads, Dc,
       out_head0, hc);
+  cudaError_t e = cudaGetLastError();
+  launch_end(4, stream);
+  return e;
+}
+
+cudaError_t launch_dkdv_reduce(const float* part, int split, int64_t part_rows, int64_t rows,
+                               int64_t row0_pos, int B, int kc, int D, int64_t S, void* dk,
+                               void* dv, int64_t dkv_rows, int64_t dkv_row0, int dkv_heads,
+                               int dkv_head0, cudaStream_t stream) {
+  const int Dc = D / 8;
+  const dim3 grid(static_cast<unsigned>((rows + kRedRows - 1) / kRedRows),
+                  static_cast<unsigned>(kc), static_cast<unsigned>(B));
+  launch_begin(4, stream);
+  dkdv_reduce_kernel<<<grid, kLayoutThreads, 0, stream>>>(
+      reinterpret_cast<const float4*>(part), split, part_rows, rows, row0_pos, B, kc, Dc, S,
+      static_cast<uint4*>(dk), static_cast<uint4*>(dv), dkv_rows, dkv_row0, dkv_heads,
+      dkv_head0);
   cudaError_t e = cudaGetLastError();
   launch_end(4, stream);
   return e;

@@ -34,7 +34,7 @@ def test_library_exports_every_declared_symbol():
     assert set(declared_functions()) == set(up.SIGNATURES), "binding and header disagree"
 
 
-def _expected_ws(B, S, Hq, Hkv, D, hc, T, kv_host, act_host=False):
+def _expected_ws(B, S, Hq, Hkv, D, hc, T, kv_host, act_host=False, causal=True):
     """The workspace arena as documented: every segment 256-byte aligned."""
     al = lambda x: (x + 255) // 256 * 256  # noqa: E731
     G = Hq // Hkv
@@ -51,6 +51,9 @@ def _expected_ws(B, S, Hq, Hkv, D, hc, T, kv_host, act_host=False):
     # pinned host memory as well)
     dkdv = 4 * al(B * kc * T * D * 2) if kv_host else 0
     bwd = 2 * al(qw) + kv + dkdv + al(B * hc * S_pad * D * 4) + 2 * al(B * hc * S_pad * 4)
+    if causal and D == 128 and G > 1 and S <= 16384:  # split backward: G fp32 dK/dV shares
+        rows = (T + 127) // 128 * 128 if kv_host else S_pad
+        bwd += al(G * B * kc * rows * 2 * D * 4)
     if act_host:  # host q/o/dout/dq: Q and dO buffer 2, 2 head-major O copies, 2 dQ stagings
         bwd += 6 * al(qw)
     return fwd, bwd
