@@ -9,6 +9,7 @@
 // Per key tile j, for query tile w in {0, 1}:
 //   S_w = Q_w K_j^T            tcgen05 (M 128, N 128, K 128) -> TMEM S[w]
 //   P_w = exp2(S_w*scale*log2e - m_w), masked; bf16, written back over S[w]'s first 64 columns
+//         (from the scores held in registers: one TMEM read of S per tile)
 //   O_w += P_w V_j             tcgen05 with A read from TMEM
 // MMA issue order: S0_0, S1_0, then per j: PV0_j, S0_{j+1}, PV1_j, S1_{j+1}. The tcgen05 pipe
 // executes one thread's MMAs in order, so S0_{j+1} overwrites S[0] only after PV0_j has read
@@ -16,8 +17,10 @@
 // sees its next S, its O accumulator is settled and may be rescaled in place.
 //
 // Threads (320): warps 0-3 softmax for tile 0, warps 4-7 for tile 1 (thread = query row = TMEM
-// lane), warp 8 TMEM + MMA issue, warp 9 TMA producer. Shared memory: Q0, Q1, two K and two V
-// stages. TMEM: S[0] 0, S[1] 128, O[0] 256, O[1] 384.
+// lane), warp 8 TMEM + MMA issue, warp 9 TMA producer. A softmax thread reads its row's 128
+// scores from TMEM once and keeps them in registers (168 per thread: ten warps share an SM's
+// four 16K-register partitions three, three, two and two). Shared memory: Q0, Q1, two K and two
+// V stages. TMEM: S[0] 0, S[1] 128, O[0] 256, O[1] 384.
 #include <cfloat>
 
 #include "internal.h"
@@ -115,6 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
 
+  if (warp >= 8) {
   if (warp == 9) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
@@ -156,20 +160,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16(128, 128, false, false);
       const uint32_t id_o = idesc_bf16(128, kD, false, true);
-      // Descriptors built once; stages and steps are constant offsets (16-byte units).
-      const uint64_t dQ0 = kdesc0(smem_u32(smem + L::kQ));
-      const uint64_t dK0 = kdesc0(smem_u32(smem + L::kK));
-      const uint64_t dV0 = mndesc0(smem_u32(smem + L::kV));
+      // One base descriptor per operand form; stages and steps are compile-time offsets (in
+      // 16-byte units), the base made opaque at each use so that no per-step descriptor is
+      // held in a register across the loop.
+      const uint64_t base_k = kdesc0(smem_u32(smem));
+      const uint64_t base_mn = mndesc0(smem_u32(smem));
       constexpr uint32_t kTileU = kTile >> 4;
+      constexpr uint32_t uQ = L::kQ >> 4, uK = L::kK >> 4, uV = L::kV >> 4;
       bool ok = wait(q_full, 0);
       auto issue_s = [&](int w, int j) -> bool {
         if (w == 0 && !wait(k_full + (j & 1), (j >> 1) & 1)) return false;
         tc_fence_after();
-        const uint64_t dQ = dQ0 + w * kTileU, dK = dK0 + (j & 1) * kTileU;
+        const uint64_t bk = opaque_u64(base_k);
+        const uint32_t uq = uQ + w * kTileU, uk = uK + (j & 1) * kTileU;
         const uint32_t tS = tmem + 128 * w;
 #pragma unroll
         for (int k16 = 0; k16 < kD / 16; ++k16)
-          umma_f16_ss(tS, dQ + kstep(k16), dK + kstep(k16), id_s, k16 > 0 ? 1u : 0u);
+          umma_f16_ss(tS, bk + (uq + kstep(k16)), bk + (uk + kstep(k16)), id_s,
+                      k16 > 0 ? 1u : 0u);
         umma_commit(s_full + w);
         return true;
       };
@@ -177,12 +185,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait(p_full + w, j & 1)) return false;
         if (w == 0 && !wait(v_full + (j & 1), (j >> 1) & 1)) return false;
         tc_fence_after();
-        const uint64_t dV = dV0 + (j & 1) * kTileU;
+        const uint64_t bmn = opaque_u64(base_mn);
+        const uint32_t uv = uV + (j & 1) * kTileU;
         const uint32_t acc0 = (j > 0 || !a.first) ? 1u : 0u;
         const uint32_t tP = tmem + 128 * w, tO = tmem + 256 + 128 * w;
 #pragma unroll
         for (int k16 = 0; k16 < 8; ++k16)
-          umma_f16_ts(tO, tP + k16 * 8, dV + mnstep(k16), id_o, k16 > 0 ? 1u : acc0);
+          umma_f16_ts(tO, tP + k16 * 8, bmn + (uv + mnstep(k16)), id_o, k16 > 0 ? 1u : acc0);
         if (j == n_kv - 1) umma_commit(o_done + w);
         return true;
       };
@@ -199,6 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(drain, 0, 100000000ull);
       }
     }
+  }
   } else {
     // ---------------- softmax groups ----------------
     const int w = warp >> 2;
@@ -247,32 +257,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         lim = a.kv_row_hi - r0;
         if (a.causal) lim = min(lim, qrow - p0 + 1);
       }
-      // Pass 1 over S (TMEM): the row maximum. Keeping the row in TMEM and reading it twice
-      // keeps the softmax within the 168 registers a 10-warp CTA allows. Only tiles that
-      // straddle the diagonal or an end pay for the mask.
-      // Four independent running maxima keep the dependent chain short (16 steps per half).
-      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      // The row's 128 scores are read from TMEM once, both 64-column halves in flight together,
+      // and stay in registers: the maximum, the exponentials and the bf16 packing all work on
+      // them (P packed in place into the low half of each array). Only tiles that straddle the
+      // diagonal or an end pay for the mask. Four independent running maxima keep the dependent
+      // chain short.
+      uint32_t ra[64], rb[64];
+      tmem_ld64_nowait(tS + lane_off, ra);
+      tmem_ld64_nowait(tS + lane_off + 64, rb);
+      tmem_wait_ld_dep64(ra);
+      tmem_reg_dep64(rb);
       if (need_mask) {
+        const int lim32 = static_cast<int>(lim < 0 ? 0 : lim);  // visible columns, <= 128
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t r[64];
-          tmem_ld64_sync(tS + lane_off + h * 64, r);
-#pragma unroll
-          for (int i = 0; i < 64; i += 2)
-            mq[(i >> 1) & 3] =
-                fmax3(mq[(i >> 1) & 3], (h * 64 + i < lim) ? __uint_as_float(r[i]) : -INFINITY,
-                      (h * 64 + i + 1 < lim) ? __uint_as_float(r[i + 1]) : -INFINITY);
+        for (int i = 0; i < 64; ++i) {
+          if (i >= lim32) ra[i] = __float_as_uint(-INFINITY);
+          if (64 + i >= lim32) rb[i] = __float_as_uint(-INFINITY);
         }
-      } else {
+      }
+      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t r[64];
-          tmem_ld64_sync(tS + lane_off + h * 64, r);
-#pragma unroll
-          for (int i = 0; i < 64; i += 2)
-            mq[(i >> 1) & 3] =
-                fmax3(mq[(i >> 1) & 3], __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
-        }
+      for (int i = 0; i < 64; i += 2) {
+        mq[(i >> 1) & 3] = fmax3(mq[(i >> 1) & 3], __uint_as_float(ra[i]), __uint_as_float(ra[i + 1]));
+        mq[((i >> 1) + 2) & 3] =
+            fmax3(mq[((i >> 1) + 2) & 3], __uint_as_float(rb[i]), __uint_as_float(rb[i + 1]));
       }
       const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
       const float m_new = fmaxf(m_used, mx * a.scale_log2);
@@ -283,7 +291,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_used = m_new;
       }
       l_sum *= alpha;
-      // O_w is settled (the commit that published S_w(j) covers PV_w(j-1)): rescale in place.
+      const float mb = (m_used == -INFINITY) ? 0.f : m_used;
+      // P rounded to bf16 once, written over S's first 64 columns (P of key columns c..c+63
+      // goes to TMEM columns c/2..c/2+31; every score is already in registers). The row sum adds
+      // the fp32 weights, in two independent chains.
+      const uint64_t sl2 = f2_pack(a.scale_log2, a.scale_log2);
+      const uint64_t nm2 = f2_pack(-mb, -mb);
+      uint64_t sum2 = f2_pack(0.f, 0.f), sum2b = f2_pack(0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        float x0, x1;
+        f2_unpack(ffma2(f2_pack_u(ra[2 * i], ra[2 * i + 1]), sl2, nm2), x0, x1);
+        const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+        ra[i] = pack_bf16(e0, e1);  // reads 2i, 2i+1 >= i first
+        sum2 = fadd2(sum2, f2_pack(e0, e1));
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        float x0, x1;
+        f2_unpack(ffma2(f2_pack_u(rb[2 * i], rb[2 * i + 1]), sl2, nm2), x0, x1);
+        const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+        rb[i] = pack_bf16(e0, e1);
+        sum2b = fadd2(sum2b, f2_pack(e0, e1));
+      }
+      {
+        uint32_t pa[32], pb[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          pa[i] = ra[i];
+          pb[i] = rb[i];
+        }
+        tmem_st32(tS + lane_off, pa);
+        tmem_st32(tS + lane_off + 32, pb);
+      }
+      // O_w is settled (the commit that published S_w(j) covers PV_w(j-1)): rescale it in place
+      // now that the scores are consumed (their registers free), before P_w(j) is published.
       const bool o_has = (j >= 1) || !a.first;
       if (o_has && __any_sync(0xffffffffu, upd)) {
 #pragma unroll
@@ -294,38 +336,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
           tmem_st32(tO + lane_off + c * 32, r);
         }
-      }
-      const float mb = (m_used == -INFINITY) ? 0.f : m_used;
-      // Pass 2: P rounded to bf16 once, written over S's first 64 columns; the row sum adds
-      // exactly the weights the P.V MMA consumes (paired fp32 adds of the two bf16 halves).
-      // Columns 64..127 are read before any P lands there (P of columns c..c+63 goes to
-      // columns c/2..c/2+31).
-      const uint64_t sl2 = f2_pack(a.scale_log2, a.scale_log2);
-      const uint64_t nm2 = f2_pack(-mb, -mb);
-      uint64_t sum2 = f2_pack(0.f, 0.f), sum2b = f2_pack(0.f, 0.f);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t r[64];
-        tmem_ld64_sync(tS + lane_off + h * 64, r);
-        if (need_mask) {
-#pragma unroll
-          for (int i = 0; i < 64; ++i)
-            if (h * 64 + i >= lim) r[i] = __float_as_uint(-INFINITY);
-        }
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float x0, x1;
-          f2_unpack(ffma2(f2_pack_u(r[2 * i], r[2 * i + 1]), sl2, nm2), x0, x1);
-          const uint32_t v = pack_bf16(ex2_approx(x0), ex2_approx(x1));
-          pk[i] = v;
-          // two independent sums halve the dependent add chain
-          if (i & 1)
-            sum2b = fadd2(sum2b, f2_pack_u(v << 16, v & 0xFFFF0000u));
-          else
-            sum2 = fadd2(sum2, f2_pack_u(v << 16, v & 0xFFFF0000u));
-        }
-        tmem_st32(tS + lane_off + h * 32, pk);
       }
       float s_lo, s_hi;
       f2_unpack(fadd2(sum2, sum2b), s_lo, s_hi);
