@@ -655,11 +655,14 @@ def run_sweep(a):
                     "kv_h2d_ms": kv_ms, "kv_h2d_trunks": kv_n,
                     "kv_h2d_gbs": kv_bytes / (kv_ms * 1e-3) / 1e9 if kv_ms else None,
                     "dkdv_d2h_ms": st["dkdv_d2h"][0], "dkdv_d2h_trunks": st["dkdv_d2h"][1],
+                    # the compute stream's stalls waiting for staged trunks: copy time not
+                    # hidden behind compute, measured directly
+                    "kv_wait_ms": st["kv_wait"][0],
                 }
                 if (hc, T) in device_ms:
-                    # what staging adds to the step over the device-resident run: the copy
-                    # time the compute stream could not hide
-                    copies["exposed_copy_ms"] = ms_step - device_ms[(hc, T)]
+                    # the whole difference to the device-resident run: copy stalls plus the
+                    # trunk-by-trunk launch structure staging needs
+                    copies["vs_device_ms"] = ms_step - device_ms[(hc, T)]
             ff, fb = w.flops_fwd() * a.steps, w.flops_bwd() * a.steps
             print(json.dumps({
                 "sweep": a.sweep, "workload": w.name, "S": w.S, "head_chunk": hc,

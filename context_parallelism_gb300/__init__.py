@@ -28,7 +28,7 @@ UPIPE_PASS_FWD, UPIPE_PASS_BWD, UPIPE_PASS_BOTH, UPIPE_PASS_FUSED = 0, 1, 2, 3
 UPIPE_HOST_KV, UPIPE_HOST_ACT = 1, 2
 
 KERNEL_CLASSES = ["layout", "attn_fwd", "bwd_pre", "attn_bwd", "dq_convert", "other",
-                  "loss_gemm", "loss_merge", "kv_h2d", "dkdv_d2h"]
+                  "loss_gemm", "loss_merge", "kv_h2d", "dkdv_d2h", "kv_wait"]
 
 # Every symbol include/upipe.h declares, with (restype, argtypes).
 _vp, _i, _i64, _sz, _u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_uint64

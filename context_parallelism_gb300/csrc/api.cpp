@@ -309,7 +309,10 @@ int make_attn_plan(int B, int64_t S, int Hq, int Hkv, int D, int causal, int hea
   // times the shortest). Up to S = 16K the walk is shared by G CTAs, one q-head each, whose
   // fp32 dK/dV shares a reduce kernel adds in a fixed order. The rule depends on the shape
   // only (not on head_chunk), so the workspace stays proportional to head_chunk.
-  if (causal && D == 128 && G > 1 && S <= 16384) {
+  // The same holds per launch with host K/V, where each key/value trunk is one launch: up to
+  // 512 key tiles per launch (T <= 64K) split too.
+  const int64_t kt_launch = (p->kv_host ? p->T_pad : p->S_pad) / 128 * B;
+  if (causal && D == 128 && G > 1 && kt_launch <= (p->kv_host ? 512 : 128)) {
     p->bwd_split = G;
     p->part_rows = p->kv_host ? p->T_pad : p->S_pad;
     p->b_dkv_part = take(static_cast<size_t>(G) * kcB * p->part_rows * 2 * D * 4);
@@ -476,7 +479,10 @@ struct Stager {
       if (st != UPIPE_OK) return st;
       ++staged;
     }
+    // bracketed when profiling: the gap is the time the compute stream stalled for the copy
+    copy_begin(compute);
     UPIPE_CUDA(cudaStreamWaitEvent(compute, ds->slot_ready[i & 1], 0));
+    copy_end(UPIPE_K_KV_WAIT, compute);
     return UPIPE_OK;
   }
   int after(int i) {
@@ -638,29 +644,31 @@ int upipe_attn_fwd(const void* q, const void* k, const void* v, void* o, float* 
   }
   // host o: group g's kernels write a [B, S, hc, D] staging buffer, copied out afterwards
   void* o_out = o;
-  // Host K/V: one launch per (key/value trunk n, query trunk m), the state in the arena.
-  auto launch = [&](const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, int h0,
-                    int m, int n, int64_t row_lo, int64_t row_hi, int64_t pos0,
-                    int64_t state_stride) -> int {
-    const int n_last = causal ? m : p.n_trunks - 1;
+  // Host K/V: one launch per key/value trunk n over every query row that sees it (rows from
+  // n*T on when causal, all rows otherwise). Each query trunk's running state sits in the
+  // S-row arena state; a tile finalises when n is its last trunk (its diagonal one when
+  // causal), the others store their state for trunk n+1.
+  auto launch_trunk = [&](const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          int h0, int n, int64_t Tn) -> int {
+    const int64_t t0 = static_cast<int64_t>(n) * p.T;
     FwdArgs a{};
-    a.q_lo = static_cast<int64_t>(m) * p.T;
-    a.q_hi = std::min<int64_t>(S, a.q_lo + p.T);
+    a.q_lo = causal ? t0 : 0;
+    a.q_hi = S;
     a.S = S;
     a.hc = p.hc; a.kc = p.kc; a.G = p.G; a.Hq = Hq; a.h0 = h0;
-    a.causal = causal; a.first = (n == 0); a.last = (n == n_last);
+    a.causal = causal; a.first = (n == 0);
+    a.last = causal || n == p.n_trunks - 1;
+    a.last_q_end = causal ? std::min<int64_t>(S, t0 + p.T) : 0;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.o = o_out; a.lse = lse;
     if (o_host) { a.o_heads = p.hc; a.o_head0 = 0; }
-    // with an S-sized state the rows of query trunk m start m*T rows in
-    const int64_t soff = state_stride ? a.q_lo : 0;
-    a.state_o = state_o ? state_o + soff * D : nullptr;
-    a.state_ml = state_ml ? state_ml + soff * 2 : nullptr;
-    // rows past the state buffer's end are never written (the last trunk may be ragged)
-    a.state_rows = state_stride ? std::min<int64_t>(p.T_pad, p.S_pad - a.q_lo) : p.T_pad;
-    a.state_stride = state_stride;
+    // the state rows of this launch start q_lo rows into the S_pad-row state
+    a.state_o = state_o ? state_o + a.q_lo * D : nullptr;
+    a.state_ml = state_ml ? state_ml + a.q_lo * 2 : nullptr;
+    a.state_rows = p.S_pad - a.q_lo;
+    a.state_stride = p.S_pad;
     a.err = ds->err;
-    a.kv_row_lo = row_lo; a.kv_row_hi = row_hi; a.kv_pos0 = pos0;
+    a.kv_row_lo = 0; a.kv_row_hi = Tn; a.kv_pos0 = t0;
     UPIPE_CUDA(launch_attn_fwd(D, B, tq, tk, tv, a, stream));
     return UPIPE_OK;
   };
@@ -703,9 +711,8 @@ int upipe_attn_fwd(const void* q, const void* k, const void* v, void* o, float* 
       UPIPE_CUDA(launch_fwd_resident(p, tq, tk, tv, h0, o_out, o_host ? p.hc : 0, lse, ds->err,
                                      stream));
     } else {
-      // Host K/V: key/value trunk n is staged once and then met by every query trunk that
-      // sees it (m >= n when causal); each query trunk keeps its running state in an S-sized
-      // buffer.
+      // Host K/V: key/value trunk n is staged once and then met, in one launch, by every
+      // query trunk that sees it (m >= n when causal).
       for (int n = 0; n < p.n_trunks; ++n, ++job) {
         const int64_t t0 = static_cast<int64_t>(n) * p.T;
         const int64_t Tn = std::min<int64_t>(p.T, S - t0);
@@ -714,10 +721,8 @@ int upipe_attn_fwd(const void* q, const void* k, const void* v, void* o, float* 
         const int s = job & 1;
         UPIPE_CUDA(make_tmap_bf16(&tk, stg.slot_k[s], D, Tn, static_cast<int64_t>(B) * p.kc));
         UPIPE_CUDA(make_tmap_bf16(&tv, stg.slot_v[s], D, Tn, static_cast<int64_t>(B) * p.kc));
-        for (int m = causal ? n : 0; m < p.n_trunks; ++m) {
-          st = launch(tq, tk, tv, h0, m, n, 0, Tn, t0, p.n_trunks > 1 ? p.S_pad : 0);
-          if (st != UPIPE_OK) return st;
-        }
+        st = launch_trunk(tq, tk, tv, h0, n, Tn);
+        if (st != UPIPE_OK) return st;
         st = stg.after(job);
         if (st != UPIPE_OK) return st;
       }

@@ -320,7 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (good) {
       const bool row_ok = qrow < a.q_hi;
-      if (a.last) {
+      const bool last = a.last && (a.last_q_end == 0 || q0 < a.last_q_end);
+      if (last) {
         const float inv_l = 1.f / l_sum;
         __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.o) +
                               ((static_cast<int64_t>(b) * a.S + qrow) * (a.o_heads ? a.o_heads : a.Hq) +

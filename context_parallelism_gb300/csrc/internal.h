@@ -113,6 +113,8 @@ struct FwdArgs {
   int64_t S;                     // sequence length
   int hc, kc, G, Hq, h0;         // group q-heads, group kv-heads, Hq/Hkv, total q-heads, first q-head
   int causal, first, last;       // first: no carried state; last: finalise O and LSE
+  int64_t last_q_end;            // with last: only query tiles starting below it are final
+                                 // (the rest store their state); 0 = every tile
   float scale_log2;              // softmax scale * log2(e)
   void* o;                       // bf16, written when last: [B,S,Hq,D], or a staging [B,S,o_heads,D]
   int o_heads, o_head0;          // heads per row of o and this group's first; 0 means Hq and h0

@@ -18,9 +18,9 @@ namespace upipe {
 namespace {
 
 constexpr int kLayoutThreads = 256;
-// Bytes one block of the gather / scatter kernels moves: 32 KiB, 8 16-byte vectors per thread,
+// Bytes one block task of the gather / scatter kernels moves: 16 KiB, 4 16-byte vectors per thread,
 // all loaded before any is stored.
-constexpr int kVecPerThread = 8;
+constexpr int kVecPerThread = 4;
 constexpr int kBlockVecs = kLayoutThreads * kVecPerThread;
 
 // Up to three head-group copies in one launch. Job j moves heads [h0, h0 + count) of a

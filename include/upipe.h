@@ -302,7 +302,9 @@ enum {
   UPIPE_K_KV_H2D = 8,     /* not a kernel: one key/value trunk staged host -> device (copy
                              stream; "launches" counts trunks) */
   UPIPE_K_DKDV_D2H = 9,   /* not a kernel: one trunk's dK/dV copied device -> host */
-  UPIPE_K_COUNT = 10
+  UPIPE_K_KV_WAIT = 10,   /* not a kernel: how long the compute stream stalled waiting for a
+                             staged key/value trunk (the copy time not hidden behind compute) */
+  UPIPE_K_COUNT = 11
 };
 
 typedef struct {
@@ -327,7 +329,8 @@ uint64_t upipe_launch_count(void);
 /*
  * Profiling: while enabled, every launch is bracketed by CUDA events recorded on the stream
  * it is launched on, and so is each key/value trunk staged in (UPIPE_K_KV_H2D) and each
- * trunk's dK/dV copied out (UPIPE_K_DKDV_D2H) on the library's copy stream.
+ * trunk's dK/dV copied out (UPIPE_K_DKDV_D2H) on the library's copy stream, and the compute
+ * stream's wait for each staged trunk (UPIPE_K_KV_WAIT).
  * upipe_profile_read() synchronises those events, adds their elapsed times into out[0..n)
  * (indexed by class) and forgets them. Returns a status code. Copies are not counted by
  * upipe_launch_count().

@@ -51,9 +51,9 @@ def _expected_ws(B, S, Hq, Hkv, D, hc, T, kv_host, act_host=False, causal=True):
     # pinned host memory as well)
     dkdv = 4 * al(B * kc * T * D * 2) if kv_host else 0
     bwd = 2 * al(qw) + kv + dkdv + al(B * hc * S_pad * D * 4) + 2 * al(B * hc * S_pad * 4)
-    if causal and D == 128 and G > 1 and S <= 16384:  # split backward: G fp32 dK/dV shares
-        rows = (T + 127) // 128 * 128 if kv_host else S_pad
-        bwd += al(G * B * kc * rows * 2 * D * 4)
+    rows = (T + 127) // 128 * 128 if kv_host else S_pad
+    if causal and D == 128 and G > 1 and rows // 128 * B <= (512 if kv_host else 128):
+        bwd += al(G * B * kc * rows * 2 * D * 4)  # split backward: G fp32 dK/dV shares
     if act_host:  # host q/o/dout/dq: Q and dO buffer 2, 2 head-major O copies, 2 dQ stagings
         bwd += 6 * al(qw)
     return fwd, bwd
