@@ -107,12 +107,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int kt = blockIdx.x;  // smallest key positions (most query tiles) first
+  // One-dimensional grid, (batch, kv-head, share) fastest: the smallest key positions (the
+  // longest causal walks) of every kv-head start first, so short launches end evenly.
   const int split = a.split > 1 ? a.split : 1;
-  const int kvl = static_cast<int>(blockIdx.y) / split;
-  const int sp = static_cast<int>(blockIdx.y) - kvl * split;  // share of the group's q-heads
-  const int gh = a.G / split;                                 // q-heads this CTA walks
-  const int b = blockIdx.z;
+  const int ny = a.kc * split;
+  const int n_kt = static_cast<int>((a.kv_row_hi - a.kv_row_lo + 127) / 128);
+  const int nb = static_cast<int>(gridDim.x) / (n_kt * ny);  // batch
+  const int kt = static_cast<int>(blockIdx.x) / (ny * nb);
+  const int yb = static_cast<int>(blockIdx.x) - kt * ny * nb;
+  const int yy = yb % ny;
+  const int b = yb / ny;
+  const int kvl = yy / split;
+  const int sp = yy - kvl * split;  // share of the group's q-heads
+  const int gh = a.G / split;       // q-heads this CTA walks
   const int64_t r0 = a.kv_row_lo + static_cast<int64_t>(kt) * 128;  // K/V map row
   const int64_t p0 = a.kv_pos0 + r0;                                // global key position
   const int zk = b * a.kc + kvl;
@@ -461,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // kernel adds the shares of the key tile's CTAs in a fixed order
       const uint32_t tAcc = w == 0 ? tDV : tDK;
       float* part = a.dkv_part +
-                    (((static_cast<int64_t>(sp) * gridDim.z + b) * a.kc + kvl) * a.part_rows +
+                    (((static_cast<int64_t>(sp) * nb + b) * a.kc + kvl) * a.part_rows +
                      (r0 - a.kv_row_lo) + t) * (2 * kD) + (w == 0 ? kD : 0);
 #pragma unroll
       for (int c = 0; c < kD / 32; ++c) {
@@ -536,8 +543,10 @@ cudaError_t launch_attn_bwd(int D, int B, const CUtensorMap& q_map, const CUtens
   const int split = a.split > 1 ? a.split : 1;
   if (a.G % split || (split > 1 && (!a.dkv_part || a.part_rows < n_kt * 128)))
     return cudaErrorInvalidValue;
-  dim3 grid(static_cast<unsigned>(n_kt), static_cast<unsigned>(a.kc * split),
-            static_cast<unsigned>(B));
+  const int64_t n_cta = n_kt * a.kc * split * B;
+  if (n_cta <= 0) return cudaSuccess;
+  if (n_cta > 0x7fffffff) return cudaErrorInvalidValue;
+  dim3 grid(static_cast<unsigned>(n_cta));
   launch_begin(3, stream);
   attn_bwd_pp_kernel<<<grid, kThreads, BppLayout::kBytes, stream>>>(q_map, do_map, k_map, v_map, a);
   cudaError_t e = cudaGetLastError();

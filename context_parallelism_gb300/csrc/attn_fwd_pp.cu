@@ -67,11 +67,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // Heaviest causal tile pairs (largest query index) are scheduled first.
-  const int pr = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);
+  // One-dimensional grid, (batch, head) fastest: the heaviest causal tile pairs (largest query
+  // index) of every head start first, before any lighter pair, so short launches end evenly.
+  const int n_pairs = static_cast<int>((a.q_hi - a.q_lo + 255) / 256);
+  const int nh = static_cast<int>(gridDim.x) / n_pairs;  // hc * B
+  const int pr = n_pairs - 1 - static_cast<int>(blockIdx.x) / nh;
+  const int hb = static_cast<int>(blockIdx.x) - (n_pairs - 1 - pr) * nh;
   const int64_t q0 = a.q_lo + static_cast<int64_t>(pr) * 256;
-  const int hl = blockIdx.y;
-  const int b = blockIdx.z;
+  const int hl = hb % a.hc;
+  const int b = hb / a.hc;
   const int zq = b * a.hc + hl;
   const int zk = b * a.kc + hl / a.G;
   int64_t kv_end = a.kv_row_hi;
@@ -415,7 +419,10 @@ cudaError_t launch_attn_fwd(int D, int B, const CUtensorMap& q_map, const CUtens
     if (e != cudaSuccess) return e;
   }
   const int64_t n_pairs = (a.q_hi - a.q_lo + 255) / 256;
-  dim3 grid(static_cast<unsigned>(n_pairs), static_cast<unsigned>(a.hc), static_cast<unsigned>(B));
+  const int64_t n_cta = n_pairs * a.hc * B;
+  if (n_cta <= 0) return cudaSuccess;
+  if (n_cta > 0x7fffffff) return cudaErrorInvalidValue;
+  dim3 grid(static_cast<unsigned>(n_cta));
   launch_begin(1, stream);
   attn_fwd_pp_kernel<<<grid, kThreads, FppLayout::kBytes, stream>>>(q_map, k_map, v_map, a);
   cudaError_t e = cudaGetLastError();

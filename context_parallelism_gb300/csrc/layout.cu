@@ -8,8 +8,8 @@
 //     log2(e) and the zeroing of the fp32 dQ accumulator, fused in one pass;
 //   * the dQ conversion: fp32 accumulator -> bf16 token-major dq.
 // Each thread moves 16-byte vectors. Blocks cover fixed runs of sequence positions of one batch
-// row (and head), so no 64-bit division is done per element; the gathers of a head group's
-// Q, K and V go in one launch.
+// row and head, so no 64-bit division is done per element; the gathers of a head group's Q, K
+// and V go in one launch.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -18,79 +18,84 @@ namespace upipe {
 namespace {
 
 constexpr int kLayoutThreads = 256;
-// Bytes one block task of the gather / scatter kernels moves: 16 KiB, 4 16-byte vectors per thread,
-// all loaded before any is stored.
+// A block task of the gather / scatter kernels moves 16 KiB: 4 16-byte vectors per thread, all
+// loaded before any is stored.
 constexpr int kVecPerThread = 4;
 constexpr int kBlockVecs = kLayoutThreads * kVecPerThread;
 
 // Up to three head-group copies in one launch. Job j moves heads [h0, h0 + count) of a
 // token-major [B, S, H, D] tensor to (or, for the scatter, from) a head-major
-// [B, count, S, D] buffer. A job is cut into blocks of `rows` consecutive sequence positions of
-// one batch row; a block's rows * count * Dc vectors are numbered (row, head, chunk), so the
-// token-major side is contiguous. All index arithmetic inside a block is 32-bit.
+// [B, count, S, D] buffer. A block task is one run of `rows` consecutive sequence positions of
+// one (batch row, head): its head-major side is one contiguous 16 KiB run, its token-major side
+// `rows` pieces of D * 2 bytes, one per position. Tasks are numbered job, then (batch, head),
+// then position run fastest, so neighbouring blocks stream neighbouring positions of a head.
 struct LayoutJobs {
   const uint4* src[3];
   uint4* dst[3];
   int H[3], h0[3], count[3];
-  int rows[3];       // sequence positions per block
-  int seq_blocks[3]; // blocks per batch row: ceil(S / rows)
-  int first_block[4];  // prefix sums of the jobs' block counts (B * seq_blocks)
+  int first_block[4];  // prefix sums of the jobs' task counts (B * count * seq_blocks)
+  int seq_blocks;      // position runs per (batch row, head): ceil(S / rows)
+  int rows;            // positions per run: kBlockVecs / Dc
+  int lg_dc;           // log2 of the 16-byte vectors per position (Dc = D / 8)
   int n_jobs;
 };
 
 template <bool kToHead>
-__device__ __forceinline__ void layout_task(const LayoutJobs& J, int64_t S, int Dc, int task) {
-  int j = 0;
-  while (j + 1 < J.n_jobs && task >= J.first_block[j + 1]) ++j;
-  const int bt = task - J.first_block[j];
-  const int b = bt / J.seq_blocks[j];
-  const int64_t s0 = static_cast<int64_t>(bt - b * J.seq_blocks[j]) * J.rows[j];
-  const int count = J.count[j], W = count * Dc;
-  const int nrows = static_cast<int>(S - s0 < J.rows[j] ? S - s0 : J.rows[j]);
-  const int n = nrows * W;
-  // token-major rows of this block start at (b*S + s0)*H + h0; head-major rows at
-  // (b*count + h)*S + s0
-  const int64_t tok0 = ((static_cast<int64_t>(b) * S + s0) * J.H[j] + J.h0[j]) * Dc;
-  const int64_t tokStride = static_cast<int64_t>(J.H[j]) * Dc;
-  const int64_t hm0 = (static_cast<int64_t>(b) * count * S + s0) * Dc;
-  const int64_t hmStride = S * Dc;
-  const uint4* __restrict__ src = J.src[j];
-  uint4* __restrict__ dst = J.dst[j];
+__global__ void __launch_bounds__(kLayoutThreads)
+    layout_kernel(const LayoutJobs J, int64_t S) {
+  const int task = static_cast<int>(blockIdx.x);
+  // the job's fields picked by selects, not by a runtime index into the parameter block
+  const int j = (task >= J.first_block[1]) + (J.n_jobs > 2 && task >= J.first_block[2]);
+  auto pick = [j](auto x0, auto x1, auto x2) { return j == 0 ? x0 : (j == 1 ? x1 : x2); };
+  const int bt = task - pick(J.first_block[0], J.first_block[1], J.first_block[2]);
+  const int hb = bt / J.seq_blocks;
+  const int sb = bt - hb * J.seq_blocks;
+  const int count = pick(J.count[0], J.count[1], J.count[2]);
+  const int H = pick(J.H[0], J.H[1], J.H[2]);
+  const int hj0 = pick(J.h0[0], J.h0[1], J.h0[2]);
+  const int b = hb / count, h = hb - b * count;
+  const int64_t s0 = static_cast<int64_t>(sb) * J.rows;
+  const int nrows = static_cast<int>(S - s0 < J.rows ? S - s0 : J.rows);
+  const int n = nrows << J.lg_dc;
+  const int Dc = 1 << J.lg_dc;
+  // head-major run: ((b * count + h) * S + s0) * Dc + i; token-major vector i of the run:
+  // ((b * S + s0 + r) * H + h0 + h) * Dc + c with r = i / Dc, c = i % Dc
+  const int64_t hm0 = ((static_cast<int64_t>(b) * count + h) * S + s0) << J.lg_dc;
+  const int64_t tok0 = ((static_cast<int64_t>(b) * S + s0) * H + hj0 + h) << J.lg_dc;
+  const int64_t tokStride = static_cast<int64_t>(H) << J.lg_dc;
+  const uint4* __restrict__ src = pick(J.src[0], J.src[1], J.src[2]);
+  uint4* __restrict__ dst = pick(J.dst[0], J.dst[1], J.dst[2]);
   uint4 v[kVecPerThread];
-  int64_t to[kVecPerThread];
 #pragma unroll
   for (int u = 0; u < kVecPerThread; ++u) {
     const int i = static_cast<int>(threadIdx.x) + u * kLayoutThreads;
     if (i < n) {
-      const int r = i / W, w = i - r * W;
-      const int h = w / Dc, c = w - h * Dc;
-      const int64_t tok = tok0 + r * tokStride + w;
-      const int64_t hm = hm0 + h * hmStride + static_cast<int64_t>(r) * Dc + c;
-      v[u] = __ldg(src + (kToHead ? tok : hm));
-      to[u] = kToHead ? hm : tok;
+      const int64_t tok = tok0 + (i >> J.lg_dc) * tokStride + (i & (Dc - 1));
+      v[u] = __ldg(src + (kToHead ? tok : hm0 + i));
     }
   }
 #pragma unroll
   for (int u = 0; u < kVecPerThread; ++u) {
     const int i = static_cast<int>(threadIdx.x) + u * kLayoutThreads;
-    if (i < n) dst[to[u]] = v[u];
+    if (i < n) {
+      const int64_t tok = tok0 + (i >> J.lg_dc) * tokStride + (i & (Dc - 1));
+      dst[kToHead ? hm0 + i : tok] = v[u];
+    }
   }
-}
-
-template <bool kToHead>
-__global__ void __launch_bounds__(kLayoutThreads)
-    layout_kernel(const LayoutJobs J, int64_t S, int Dc) {
-  // A fixed grid of a few blocks per SM loops over the block tasks (no block turnover).
-  for (int task = blockIdx.x; task < J.first_block[J.n_jobs]; task += gridDim.x)
-    layout_task<kToHead>(J, S, Dc, task);
 }
 
 cudaError_t launch_layout(bool to_head, const void* const* src, void* const* dst, const int* H,
                           const int* h0, const int* count, int n_jobs, int B, int64_t S, int D,
                           cudaStream_t stream) {
   const int Dc = D / 8;
+  if (Dc != 8 && Dc != 16) return cudaErrorInvalidValue;
   LayoutJobs J{};
   J.n_jobs = n_jobs;
+  J.lg_dc = Dc == 16 ? 4 : 3;
+  J.rows = kBlockVecs / Dc;
+  const int64_t sb = (S + J.rows - 1) / J.rows;
+  if (sb > (int64_t(1) << 30)) return cudaErrorInvalidValue;
+  J.seq_blocks = static_cast<int>(sb);
   int64_t total = 0;
   for (int j = 0; j < n_jobs; ++j) {
     J.src[j] = static_cast<const uint4*>(src[j]);
@@ -98,26 +103,18 @@ cudaError_t launch_layout(bool to_head, const void* const* src, void* const* dst
     J.H[j] = H[j];
     J.h0[j] = h0[j];
     J.count[j] = count[j];
-    const int W = count[j] * Dc;
-    J.rows[j] = kBlockVecs / W > 0 ? kBlockVecs / W : 1;
-    const int64_t sb = (S + J.rows[j] - 1) / J.rows[j];
-    if (W > kBlockVecs || sb * B > (int64_t(1) << 30)) return cudaErrorInvalidValue;
-    J.seq_blocks[j] = static_cast<int>(sb);
     J.first_block[j] = static_cast<int>(total);
-    total += sb * B;
+    total += sb * B * count[j];
+    if (total > (int64_t(1) << 31) - 1) return cudaErrorInvalidValue;
   }
   J.first_block[n_jobs] = static_cast<int>(total);
-  if (total > (int64_t(1) << 31) - 1) return cudaErrorInvalidValue;
-  int dev = 0, sms = 152;
-  if (cudaGetDevice(&dev) == cudaSuccess)
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  // 8 resident blocks of 256 threads per SM
-  const unsigned grid = static_cast<unsigned>(total < 8LL * sms ? total : 8LL * sms);
+  if (total == 0) return cudaSuccess;
+  const unsigned grid = static_cast<unsigned>(total);
   launch_begin(0, stream);
   if (to_head)
-    layout_kernel<true><<<grid, kLayoutThreads, 0, stream>>>(J, S, Dc);
+    layout_kernel<true><<<grid, kLayoutThreads, 0, stream>>>(J, S);
   else
-    layout_kernel<false><<<grid, kLayoutThreads, 0, stream>>>(J, S, Dc);
+    layout_kernel<false><<<grid, kLayoutThreads, 0, stream>>>(J, S);
   cudaError_t e = cudaGetLastError();
   launch_end(0, stream);
   return e;
