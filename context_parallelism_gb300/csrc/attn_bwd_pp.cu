@@ -29,14 +29,18 @@
 // and releases the columns dP(i+1) reuses. One thread's MMAs execute in order, so S(i+1)
 // overwrites S only after dV(i) has read P^T(i); the commit that publishes dP(i+1) also covers
 // dK(i) and dQ(i), which read the single dS^T buffer the groups then overwrite; and the commit
-// that frees a dO stage (after dV(i+1)) covers dP(i+1), its other reader.
+// that frees the dO stage (after dV(i+1)) covers dP(i+1), its other reader. Q has three stages
+// and dO one: Q(i+1) must be resident when S(i+1) is issued, at the top of the tile, and a
+// third stage lets its load start a whole tile earlier (Q(i+1) overwrites Q(i-2)); dO(i+1) is
+// needed only by dP(i+1), after S(i+1), dQ(i) and dK(i), which leaves its load time enough.
 //
 // Threads (512): warps 0-3 compute group 0, warps 4-7 compute group 1, warps 8-11 dQ drain,
 // warp 12 TMEM + MMA issue, warp 13 TMA producer, warps 14-15 idle. Registers move from the
 // MMA/TMA warpgroup to the compute groups and the drain (152 / 152 / 152 / 56 per thread).
 // TMEM: dV [0,128), dK [128,256), S [256,384), dP/dQ [384,512).
-// Shared memory (231.6 KB, no alignment slack: the dynamic window must start 1 KiB-aligned,
-// which is checked): K, V, two Q and two dO stages, dS^T, two LSE/D vector stages, barriers.
+// Shared memory (226 KB, no alignment slack to spare: the dynamic window must start 1 KiB-
+// aligned, which is checked): K, V, three Q stages, one dO stage, dS^T, two LSE/D vector
+// stages (each freed by both groups' dS of its tile), barriers.
 #include <cfloat>
 
 #include "internal.h"
@@ -52,12 +56,12 @@ constexpr int kTile = 128 * kD * 2;  // 32 KiB
 struct BppLayout {
   static constexpr int kK = 0;
   static constexpr int kV = kK + kTile;
-  static constexpr int kQ = kV + kTile;         // 2 stages
-  static constexpr int kDO = kQ + 2 * kTile;    // 2 stages
-  static constexpr int kDS = kDO + 2 * kTile;   // 2 boxes: query columns 0-63, 64-127
+  static constexpr int kQ = kV + kTile;         // 3 stages
+  static constexpr int kDO = kQ + 3 * kTile;    // 1 stage
+  static constexpr int kDS = kDO + kTile;       // 2 boxes: query columns 0-63, 64-127
   static constexpr int kVec = kDS + kTile;      // 2 stages x (128 LSE2 + 128 D) fp32
   static constexpr int kBar = kVec + 2 * 1024;
-  static constexpr int kNumBars = 17;
+  static constexpr int kNumBars = 19;
   static constexpr int kSlot = kBar + kNumBars * 8;
   static constexpr int kAbort = kSlot + 4;
   static constexpr int kBytes = kAbort + 4;
@@ -90,10 +94,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint64_t* kv_full = bar;
-  uint64_t* qf = bar + 1;        // [2] Q + LSE/D stage landed
-  uint64_t* df = bar + 3;        // [2] dO stage landed
-  uint64_t* qe = bar + 5;        // [2] Q stage free (after dK)
-  uint64_t* de = bar + 7;        // [2] dO stage free (after dV)
+  uint64_t* qf = bar + 1;        // [3] Q stage (and its tile's LSE/D vectors) landed
+  uint64_t* qe = bar + 4;        // [3] Q stage free (after dK)
+  uint64_t* df = bar + 7;        // dO landed
+  uint64_t* de = bar + 8;        // dO free (after dV)
   uint64_t* s_full = bar + 9;
   uint64_t* dp_full = bar + 10;
   uint64_t* dq_full = bar + 11;
@@ -102,6 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* dq_free = bar + 14;  // 4 drain-warp arrivals
   uint64_t* done = bar + 15;
   uint64_t* drain = bar + 16;
+  uint64_t* vfree = bar + 17;    // [2] LSE/D vector stage read by both groups (8 warp arrivals)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kSlot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
 
@@ -130,12 +135,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < 3; ++s) {
       mbar_init(qf + s, 1);
-      mbar_init(df + s, 1);
       mbar_init(qe + s, 1);
-      mbar_init(de + s, 1);
     }
+    mbar_init(df, 1);
+    mbar_init(de, 1);
+    mbar_init(vfree, 8);
+    mbar_init(vfree + 1, 8);
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
     mbar_init(dq_full, 1);
@@ -199,34 +206,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       int q_issued = 0, d_issued = 0;
       bool ok = true;
       Cursor cur;
+      int st = 0, sq = 0;  // Q stage it % 3 and its use count it / 3
       for (int it = 0; it < n_it; ++it, cur.next(nq)) {
-        const int st = it & 1;
         int zq;
         int64_t q0;
         decode(cur, zq, q0);
-        if (it >= 2 && !wait(qe + st, ((it >> 1) - 1) & 1)) { ok = false; break; }
+        // Q(it) overwrites Q(it - 3), last read by dK(it - 3); its LSE/D vectors overwrite
+        // tile it - 2's, last read by the groups' dS(it - 2)
+        if (it >= 3 && !wait(qe + st, (sq - 1) & 1)) { ok = false; break; }
+        if (it >= 2 && !wait(vfree + (it & 1), ((it >> 1) - 1) & 1)) { ok = false; break; }
         mbar_arrive_expect_tx(qf + st, kTile + 1024);
         for (int x = 0; x < 2; ++x)
           tma_load_3d(smem + L::kQ + st * kTile + x * kBoxBytes, &tm_q, x * 64,
                       static_cast<int>(q0), zq, qf + st);
         const int64_t vo = static_cast<int64_t>(zq) * a.S_pad + q0;
-        uint8_t* vec = smem + L::kVec + st * 1024;
+        uint8_t* vec = smem + L::kVec + (it & 1) * 1024;
         bulk_load(vec, a.lse2 + vo, 512, qf + st);
         bulk_load(vec + 512, a.dvec + vo, 512, qf + st);
         q_issued = it + 1;
-        if (it >= 2 && !wait(de + st, ((it >> 1) - 1) & 1)) { ok = false; break; }
-        mbar_arrive_expect_tx(df + st, kTile);
+        // dO(it) goes into the single dO stage once dV(it - 1) has read it
+        if (it >= 1 && !wait(de, (it - 1) & 1)) { ok = false; break; }
+        mbar_arrive_expect_tx(df, kTile);
         for (int x = 0; x < 2; ++x)
-          tma_load_3d(smem + L::kDO + st * kTile + x * kBoxBytes, &tm_do, x * 64,
-                      static_cast<int>(q0), zq, df + st);
+          tma_load_3d(smem + L::kDO + x * kBoxBytes, &tm_do, x * 64, static_cast<int>(q0), zq, df);
         d_issued = it + 1;
+        if (++st == 3) {
+          st = 0;
+          ++sq;
+        }
       }
       mbar_wait(kv_full, 0, ok ? kWaitLimitNs : 100000000ull);
       if (!ok) {  // let every load already issued land before the CTA can exit
-        for (int it = (q_issued > 2 ? q_issued - 2 : 0); it < q_issued; ++it)
-          mbar_wait(qf + (it & 1), (it >> 1) & 1, 100000000ull);
-        for (int it = (d_issued > 2 ? d_issued - 2 : 0); it < d_issued; ++it)
-          mbar_wait(df + (it & 1), (it >> 1) & 1, 100000000ull);
+        for (int it = (q_issued > 3 ? q_issued - 3 : 0); it < q_issued; ++it)
+          mbar_wait(qf + it % 3, (it / 3) & 1, 100000000ull);
+        if (d_issued > 0) mbar_wait(df, (d_issued - 1) & 1, 100000000ull);
       }
     }
   } else if (warp == 12) {
@@ -247,8 +260,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = wait(kv_full, 0);
 
       auto issue_s = [&](int i) -> bool {
-        const int st = i & 1;
-        if (!wait(qf + st, (i >> 1) & 1)) return false;
+        const int st = i % 3;
+        if (!wait(qf + st, (i / 3) & 1)) return false;
         tc_fence_after();
         const uint64_t bk = opaque_u64(base_k);
         const uint32_t uq = uQ + st * kStageU;
@@ -260,27 +273,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       auto issue_dv = [&](int i) -> bool {
-        const int st = i & 1;
         if (!wait(p_ready, i & 1)) return false;
-        if (!wait(df + st, (i >> 1) & 1)) return false;
+        if (!wait(df, i & 1)) return false;
         tc_fence_after();
         const uint64_t bmn = opaque_u64(base_mn);
-        const uint32_t udo = uDO + st * kStageU;
+        const uint32_t udo = uDO;
         const uint32_t acc0 = i > 0 ? 1u : 0u;
 #pragma unroll
         for (int k16 = 0; k16 < 8; ++k16)  // group 0's P^T at S+0, group 1's at S+64
           umma_f16_ts(tDV, tS + (k16 >> 2) * 64 + (k16 & 3) * 8, bmn + (udo + mnstep(k16)),
                       id_kmn, k16 > 0 ? 1u : acc0);
-        umma_commit(de + st);
+        umma_commit(de);
         return true;
       };
       auto issue_dp = [&](int i) -> bool {
-        const int st = i & 1;
         if (i >= 1 && !wait(dq_free, (i - 1) & 1)) return false;
-        if (!wait(df + st, (i >> 1) & 1)) return false;
+        if (!wait(df, i & 1)) return false;
         tc_fence_after();
         const uint64_t bk = opaque_u64(base_k);
-        const uint32_t udo = uDO + st * kStageU;
+        const uint32_t udo = uDO;
 #pragma unroll
         for (int k16 = 0; k16 < 8; ++k16)
           umma_f16_ss(tDP, bk + (uV + kstep(k16)), bk + (udo + kstep(k16)), id_kk,
@@ -289,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       auto issue_dk_dq = [&](int i) -> bool {
-        const int st = i & 1;
+        const int st = i % 3;
         if (!wait(ds_ready, i & 1)) return false;
         tc_fence_after();
         const uint64_t bmn = opaque_u64(base_mn);
@@ -371,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     Cursor cur_p;  // the tile do_p handles next
     // P^T(i) of this group's columns: S^T -> exp2 -> bf16 back into its own S columns.
     auto do_p = [&](int i) -> bool {
-      const int st = i & 1;
+      const int st = i & 1;  // LSE/D vector stage
       int zq;
       int64_t q0;
       decode(cur_p, zq, q0);
@@ -380,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* lse_s = reinterpret_cast<const float*>(smem + L::kVec + st * 1024) + 64 * w;
       // qf: the LSE/D vectors of this tile landed (the stage is refilled only after dK(i),
       // which needs this group's ds_ready).
-      if (!__all_sync(0xffffffffu, wait(qf + st, (i >> 1) & 1) && wait(s_full, i & 1)))
+      if (!__all_sync(0xffffffffu, wait(qf + i % 3, (i / 3) & 1) && wait(s_full, i & 1)))
         return false;
       tc_fence_after();
       const bool need_mask = (a.causal && qc0 < p0 + 127) || (qc0 + 64 > a.S) ||
@@ -449,7 +460,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(ds_ready);
+      if (lane == 0) {
+        mbar_arrive(ds_ready);
+        mbar_arrive(vfree + (i & 1));
+      }
       return true;
     };
     // Software-pipelined per group: dS(i), then P(i+1), which overlaps dK(i) and dQ(i) on the
