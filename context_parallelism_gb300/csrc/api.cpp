@@ -16,6 +16,7 @@
 //   internal copy stream, one trunk ahead of the compute stream, with events ordering slot
 //   reuse (FPDT Key Findings items 2-3 and Technical Deep Dive: host offload + double buffer,
 //   separate streams for compute and host<->device copies).
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
@@ -194,6 +195,19 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return g_encode;
 }
 }  // namespace
+
+int launch_band(int64_t units_per_lane, int lanes) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 1;
+  if (units_per_lane < 1 || lanes < 1) return 1;
+  // at least eight waves of units per band, and bands of equal size (a short last band would
+  // start its heavy units late and end alone)
+  const int64_t min_band = (8 * static_cast<int64_t>(sms) + units_per_lane - 1) / units_per_lane;
+  const int64_t n_bands = std::max<int64_t>(1, lanes / std::max<int64_t>(1, min_band));
+  return static_cast<int>((lanes + n_bands - 1) / n_bands);
+}
 
 cudaError_t make_tmap_bf16(CUtensorMap* map, const void* base, int64_t cols, int64_t rows,
                            int64_t depth, int box_rows) {

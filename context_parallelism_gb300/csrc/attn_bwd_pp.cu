@@ -112,14 +112,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // One-dimensional grid, (batch, kv-head, share) fastest: the smallest key positions (the
-  // longest causal walks) of every kv-head start first, so short launches end evenly.
+  // One-dimensional grid over (key tile, lane), lane = (batch, kv-head, share) and the
+  // smallest key positions (the longest causal walks) first, in bands of a.band lanes: inside
+  // a band the lanes' key tiles interleave, the band's longest walks first; bands follow one
+  // another.
   const int split = a.split > 1 ? a.split : 1;
   const int ny = a.kc * split;
   const int n_kt = static_cast<int>((a.kv_row_hi - a.kv_row_lo + 127) / 128);
   const int nb = static_cast<int>(gridDim.x) / (n_kt * ny);  // batch
-  const int kt = static_cast<int>(blockIdx.x) / (ny * nb);
-  const int yb = static_cast<int>(blockIdx.x) - kt * ny * nb;
+  int kt, yb;
+  {
+    const int L = static_cast<int>(blockIdx.x), lanes = ny * nb;
+    const int band = L / (a.band * n_kt);
+    const int lane0 = band * a.band;
+    const int bl = min(a.band, lanes - lane0);  // lanes of this band
+    const int u = L - lane0 * n_kt;
+    kt = u / bl;
+    yb = lane0 + (u - kt * bl);
+  }
   const int yy = yb % ny;
   const int b = yb / ny;
   const int kvl = yy / split;
@@ -561,8 +571,11 @@ cudaError_t launch_attn_bwd(int D, int B, const CUtensorMap& q_map, const CUtens
   if (n_cta <= 0) return cudaSuccess;
   if (n_cta > 0x7fffffff) return cudaErrorInvalidValue;
   dim3 grid(static_cast<unsigned>(n_cta));
+  BwdArgs args = a;
+  args.band = launch_band(n_kt, a.kc * split * B);
   launch_begin(3, stream);
-  attn_bwd_pp_kernel<<<grid, kThreads, BppLayout::kBytes, stream>>>(q_map, do_map, k_map, v_map, a);
+  attn_bwd_pp_kernel<<<grid, kThreads, BppLayout::kBytes, stream>>>(q_map, do_map, k_map, v_map,
+                                                                     args);
   cudaError_t e = cudaGetLastError();
   launch_end(3, stream);
   return e;

@@ -67,12 +67,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // One-dimensional grid, (batch, head) fastest: the heaviest causal tile pairs (largest query
-  // index) of every head start first, before any lighter pair, so short launches end evenly.
+  // One-dimensional grid over (query-tile pair, lane), lane = (batch, head) and the heaviest
+  // causal pairs (largest query index) first, in bands of a.band lanes: inside a band the
+  // lanes' pairs interleave, the band's heaviest first; bands follow one another.
   const int n_pairs = static_cast<int>((a.q_hi - a.q_lo + 255) / 256);
   const int nh = static_cast<int>(gridDim.x) / n_pairs;  // hc * B
-  const int pr = n_pairs - 1 - static_cast<int>(blockIdx.x) / nh;
-  const int hb = static_cast<int>(blockIdx.x) - (n_pairs - 1 - pr) * nh;
+  int pr, hb;
+  {
+    const int L = static_cast<int>(blockIdx.x);
+    const int band = L / (a.band * n_pairs);
+    const int lane0 = band * a.band;
+    const int bl = min(a.band, nh - lane0);  // lanes of this band
+    const int u = L - lane0 * n_pairs;
+    pr = n_pairs - 1 - u / bl;
+    hb = lane0 + (u - (n_pairs - 1 - pr) * bl);
+  }
   const int64_t q0 = a.q_lo + static_cast<int64_t>(pr) * 256;
   const int hl = hb % a.hc;
   const int b = hb / a.hc;
@@ -423,8 +432,10 @@ cudaError_t launch_attn_fwd(int D, int B, const CUtensorMap& q_map, const CUtens
   if (n_cta <= 0) return cudaSuccess;
   if (n_cta > 0x7fffffff) return cudaErrorInvalidValue;
   dim3 grid(static_cast<unsigned>(n_cta));
+  FwdArgs args = a;
+  args.band = launch_band(n_pairs, a.hc * B);
   launch_begin(1, stream);
-  attn_fwd_pp_kernel<<<grid, kThreads, FppLayout::kBytes, stream>>>(q_map, k_map, v_map, a);
+  attn_fwd_pp_kernel<<<grid, kThreads, FppLayout::kBytes, stream>>>(q_map, k_map, v_map, args);
   cudaError_t e = cudaGetLastError();
   launch_end(1, stream);
   return e;

@@ -123,8 +123,19 @@ struct FwdArgs {
   float* state_ml;               // [B*hc][state_stride][2] fp32 running max (log2 units), sum
   int64_t state_rows;            // rows of this launch's state (rows past it are never stored)
   int64_t state_stride;          // rows per head in the state buffers; 0 means state_rows
+  int band;                      // launch order, set by launch_attn_fwd (see launch_band)
   uint32_t* err;                 // device status word
 };
+
+// Launch order of the attention kernels. A launch is `lanes` independent sequences of work
+// units (a head's query-tile pairs, a kv-head's key tiles), each ordered heaviest first. Lanes
+// go in bands of `band` lanes: inside a band the units interleave across lanes, heaviest of
+// every lane first; bands run one after the other. A band holds at least eight waves of units
+// on the current device and the bands are of equal size, so long launches run a lane or two at
+// a time (their CTAs share Q/dO or K/V tiles in L2: interleaving the eight kv-heads of a 256K,
+// 64-head backward ran at two thirds of the speed) and short ones interleave every lane (no
+// lane's heavy units start last).
+int launch_band(int64_t units_per_lane, int lanes);
 
 // q_map: Q workspace [B*hc][S][D]; k_map / v_map: [B*kc][kv_rows][D].
 cudaError_t launch_attn_fwd_generic(int D, int B, const CUtensorMap& q_map,
@@ -167,6 +178,7 @@ struct BwdArgs {
   int split;
   float* dkv_part;
   int64_t part_rows;
+  int band;                      // launch order, set by launch_attn_bwd (see launch_band)
   uint32_t* err;
 };
 
