@@ -307,17 +307,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float mb = (m_used == -INFINITY) ? 0.f : m_used;
       // P rounded to bf16 once, written over S's first 64 columns (P of key columns c..c+63
       // goes to TMEM columns c/2..c/2+31; every score is already in registers). The row sum adds
-      // the fp32 weights, in two independent chains.
+      // the same bf16 weights the P.V MMA multiplies, in four independent chains, so that O's
+      // numerator and denominator agree: a row dominated by one key then gives that key's V
+      // up to the output's own rounding, whatever the weight's rounding.
       const uint64_t sl2 = f2_pack(a.scale_log2, a.scale_log2);
       const uint64_t nm2 = f2_pack(-mb, -mb);
-      uint64_t sum2 = f2_pack(0.f, 0.f), sum2b = f2_pack(0.f, 0.f);
+      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         float x0, x1;
         f2_unpack(ffma2(f2_pack_u(ra[2 * i], ra[2 * i + 1]), sl2, nm2), x0, x1);
         const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
         ra[i] = pack_bf16(e0, e1);  // reads 2i, 2i+1 >= i first
-        sum2 = fadd2(sum2, f2_pack(e0, e1));
+        add_bf16x2(s0, s1, ra[i]);
       }
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
@@ -325,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         f2_unpack(ffma2(f2_pack_u(rb[2 * i], rb[2 * i + 1]), sl2, nm2), x0, x1);
         const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
         rb[i] = pack_bf16(e0, e1);
-        sum2b = fadd2(sum2b, f2_pack(e0, e1));
+        add_bf16x2(s2, s3, rb[i]);
       }
       {
         uint32_t pa[32], pb[32];
@@ -350,10 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(tO + lane_off + c * 32, r);
         }
       }
-      float s_lo, s_hi;
-      f2_unpack(fadd2(sum2, sum2b), s_lo, s_hi);
-      const float sum = s_lo + s_hi;
-      l_sum += sum;
+      l_sum += (s0 + s1) + (s2 + s3);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();

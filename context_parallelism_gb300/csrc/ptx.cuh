@@ -396,6 +396,15 @@ __device__ __forceinline__ void red_add_f32(float* addr, float v) {
 }
 
 
+// s_lo += the low bf16 of p, s_hi += the high one, each converted to fp32 exactly
+// (mixed-precision adds: no unpacking instructions).
+__device__ __forceinline__ void add_bf16x2(float& s_lo, float& s_hi, uint32_t p) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(s_lo), "+f"(s_hi)
+      : "r"(p));
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
