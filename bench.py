@@ -73,17 +73,18 @@ def _args():
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch, from a one-pass ncu
 # capture of the first launch of each attention kernel on the default workload (one launch =
-# one head group over the whole sequence). A figure holds only for the kernel source file it was
+# one head group over the whole sequence; ncu printed these two in GB and MB to three
+# significant figures). A figure holds only for the kernel source file it was
 # taken on (by SHA-256) and for that workload; otherwise the bench reports null.
 TRAFFIC = {
     "attn_bwd": {"workload": "llama8b_s128k", "head_chunk": 8, "seq_trunk": 131072,
                  "files": ["context_parallelism_gb300/csrc/attn_bwd_pp.cu"],
-                 "sha256": "6d7d465475a91a26801257865763f35b361536eff2a92e9d7957bd9c27f24b34",
-                 "bytes": 4308017408 + 2163678464},
+                 "sha256": "8c3a428d82d25b4312eb8dbaa3d6875f5f292b8189bd9fce9eee8faf92ff7549",
+                 "bytes": 8_090_000_000 + 4_000_000_000},
     "attn_fwd": {"workload": "llama8b_s128k", "head_chunk": 8, "seq_trunk": 131072,
                  "files": ["context_parallelism_gb300/csrc/attn_fwd_pp.cu"],
-                 "sha256": "0fc8f248f8edfa9bb850c818a8d0491a4d0934cced9ead929024e61b5c60f791",
-                 "bytes": 919404288 + 255160320},
+                 "sha256": "93229bb574184d13c422be91979798dc0c1c9378df0e312d2c854d17e2250521",
+                 "bytes": 696_250_000 + 235_360_000},
     # the sequence-tiled GEMMs (one class, one kernel with several epilogues), one entry per
     # workload; the schedule key is (seq_tile, None) and the figure is the mean over one
     # step's launches. Loss, per 8192-token tile: forward logits 2.21 GB, backward recompute
@@ -93,13 +94,13 @@ TRAFFIC = {
         {"workload": "llama8b_readout_s128k", "head_chunk": 8192, "seq_trunk": None,
          "files": ["context_parallelism_gb300/csrc/gemm_tc.cu",
                    "context_parallelism_gb300/csrc/seqtile_api.cpp"],
-         "sha256": "b112e92702e28c192d3ce6c51c282e2f3308cedf620d5209a1dae5ce2e8406a8",
-         "bytes": 5925529448},
+         "sha256": "5b0cf150e036e4cdb96d44b4d44b8dadbc20c1104278578e50a0d005ae7919c6",
+         "bytes": 5925325980},
         {"workload": "llama8b_mlp_s128k", "head_chunk": 8192, "seq_trunk": None,
          "files": ["context_parallelism_gb300/csrc/gemm_tc.cu",
                    "context_parallelism_gb300/csrc/seqtile_api.cpp"],
-         "sha256": "b112e92702e28c192d3ce6c51c282e2f3308cedf620d5209a1dae5ce2e8406a8",
-         "bytes": 1366615122},
+         "sha256": "5b0cf150e036e4cdb96d44b4d44b8dadbc20c1104278578e50a0d005ae7919c6",
+         "bytes": 1367694834},
     ],
 }
 

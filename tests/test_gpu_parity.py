@@ -186,6 +186,23 @@ def test_rising_scores_force_rescales():
                "rising scores")
 
 
+@pytest.mark.parametrize("D", [128, 64])
+def test_constant_values_come_back_exactly_with_peaky_keys(D):
+    """With V the same vector at every position of a kv-head, every softmax row averages that
+    vector: O = V exactly, whatever the weights (the oracle's constant-V pin). The kernel
+    divides the P.V product by the sum of the same bf16-rounded weights it multiplied, so it
+    returns V bit for bit here, also on rows carried by one of the x8 keys, where the dominant
+    weight is far from a power of two."""
+    w = WORKLOADS["gqa32b_s256k_peaky"].with_(S=1000, Hq=8, Hkv=2, D=D, seed=43)
+    q, k, v, _ = make_inputs(w, "cpu")
+    v = v[:, :1].expand_as(v).contiguous()
+    o, _ = up.attention_forward(q.cuda(), k.cuda(), v.cuda(), causal=True, head_chunk=4,
+                                seq_trunk=1000)
+    up.upipe_sync_status()
+    want = v.repeat_interleave(w.Hq // w.Hkv, dim=2)
+    assert torch.equal(o.cpu(), want)
+
+
 @pytest.mark.parametrize("q_host,o_host,kv_host", [(True, False, False), (False, True, False),
                                                      (True, True, True)])
 def test_host_q_and_o_forward(q_host, o_host, kv_host):
